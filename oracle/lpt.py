@@ -1,0 +1,83 @@
+"""Cost-aware longest-processing-time-first (LPT) allocation of KV blocks to shards.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Follows the Split-KV knowledge card (kongchang.com), "Timeline" and "All
+Facts": context KV blocks are allocated to CP ranks by a cost-aware LPT rule,
+with a load imbalance below 1%.  The card defines neither the cost, the tie
+order nor the imbalance rate; the readings taken here are:
+
+* cost of a block = number of (query, key) pairs inside it that the attention
+  mask leaves visible.  For a fully visible block that is q_len x tokens in the
+  block; for the block holding a causal tail it counts the triangle.
+* blocks are numbered globally, sequence after sequence, logical block order
+  within a sequence.  LPT takes them by cost, largest first, equal costs by
+  lower global number, and puts each on the shard with the smallest load so
+  far, equal loads going to the lower shard id.  Loads are integers, so no
+  floating-point tie can arise.
+* imbalance rate = max load / mean load - 1.
+"""
+
+import numpy as np
+
+from .attn import visible_keys
+
+
+def block_costs(q_len, kv_len, block_len, causal):
+    """Cost of every KV block, in global block order.
+
+    Block j of sequence b holds keys [j*block_len, min((j+1)*block_len, kv_len)).
+    Its cost is the number of (query t, key k) pairs with k in the block and k
+    visible to t.
+    """
+    costs = []
+    for lq, lk in zip(q_len, kv_len):
+        lq, lk = int(lq), int(lk)
+        vis = np.array([visible_keys(lq, lk, t, causal) for t in range(lq)], dtype=np.int64)
+        n_blocks = -(-lk // block_len)
+        for j in range(n_blocks):
+            lo = j * block_len
+            hi = min(lk, lo + block_len)
+            seen = np.clip(np.minimum(vis, hi) - lo, 0, None)
+            costs.append(int(seen.sum()))
+    return costs
+
+
+def lpt_assign(costs, n_shards):
+    """LPT: largest block first, each onto the currently least-loaded shard.
+
+    Returns (shard_of_block list[int], load list[int]).
+    """
+    order = sorted(range(len(costs)), key=lambda g: (-int(costs[g]), g))
+    load = [0] * n_shards
+    shard_of_block = [-1] * len(costs)
+    for g in order:
+        best = 0
+        for s in range(1, n_shards):
+            if load[s] < load[best]:
+                best = s
+        shard_of_block[g] = best
+        load[best] += int(costs[g])
+    return shard_of_block, load
+
+
+def imbalance(load):
+    """max / mean - 1 of the shard loads (0 for a perfectly even plan)."""
+    mean = sum(load) / len(load)
+    if mean == 0:
+        return 0.0
+    return max(load) / mean - 1.0
+
+
+def shard_key_sets(shard_of_block, kv_len, block_len, n_shards):
+    """Per shard, per sequence: the logical blocks the plan put on that shard.
+
+    Returns key_sets[s][b] = sorted list of logical block indices.
+    """
+    sets = [[[] for _ in kv_len] for _ in range(n_shards)]
+    g = 0
+    for b, lk in enumerate(kv_len):
+        for j in range(-(-int(lk) // block_len)):
+            sets[shard_of_block[g]][b].append(j)
+            g += 1
+    return sets
