@@ -1,0 +1,452 @@
+"""Benchmark of the split-KV attention path on GB300: one JSON line on rank 0.
+
+A step is one pass of the whole path over one batch of resident synthetic
+input: block costs -> LPT plan -> work lists (host) -> work upload ->
+partial attention -> merge (device).  Default workload: batched decode
+(B=8, Hq=32, Hkv=8, d=128, one query per sequence over 32768 keys, bf16, paged
+block_len 256, 16 shards), whose metric is K/V read bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+                    [--impl ours|reference] [--kernel auto|simt|decode|tc]
+
+--gpus N > 1 runs under torchrun with one process per GPU; every rank solves
+its own copy of the workload (replicas; the path has no cross-GPU exchange on
+one device), value = all ranks' bytes / max-over-ranks time.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Split-KV attn fwd TFLOP/s & KV-read GB/s vs GB300 roofline, short-Q/long-KV"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "decode", "tc"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------- distributed
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def finish(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(dist_ctx, local_seconds, local_units, device=None):
+    """Max of the per-rank times and sum of the per-rank units over all ranks."""
+    if dist_ctx.pg is None:
+        return local_seconds, local_units
+    import torch
+
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist_ctx.pg.all_reduce(t, op=dist_ctx.pg.ReduceOp.MAX)
+    dist_ctx.pg.all_reduce(u, op=dist_ctx.pg.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# -------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id, path):
+        self.gpu_id, self.path, self.proc = gpu_id, path, None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        return self.summary()
+
+    def summary(self):
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def gpu_nvsmi_id(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # pragma: no cover - older torch
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# -------------------------------------------------------------- accounting
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_accounting(w, q_len, kv_len, block_cost, part_rows):
+    """Algorithmic flops and bytes of one pass (see the module docstring of DESIGN)."""
+    pairs = int(np.sum(block_cost))  # visible (query token, key) pairs, per query head
+    flops = 4.0 * w.d * w.Hq * pairs
+    kv_bytes = float(sum(kv_len)) * w.Hkv * w.d * 2 * w.elem_bytes
+    q_bytes = float(sum(q_len)) * w.Hq * w.d * w.elem_bytes
+    part_bytes = float(part_rows) * w.Hq * (w.d + 1) * 4
+    return {"flops": flops, "kv_bytes": kv_bytes, "q_bytes": q_bytes, "part_bytes": part_bytes,
+            "partial_bytes": kv_bytes + q_bytes + part_bytes}
+
+
+def traffic_for(kernel_name, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel_name}/{workload}")
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    import hashlib
+
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != e["sha256"]:
+        return None
+    return float(e["bytes_per_launch"])
+
+
+# -------------------------------------------------------------- our arm
+
+
+def run_ours(args, dctx):
+    import torch
+
+    from context_long_attention_lpt_gb300 import splitkv as K
+    from context_long_attention_lpt_gb300 import workloads as wl
+    from context_long_attention_lpt_gb300.runner import SplitKVAttention
+
+    dctx.init("nccl")
+    dev = dctx.local_rank
+    torch.cuda.set_device(dev)
+    K.lib()
+    w = wl.WORKLOADS[args.workload]
+    kernel = {"auto": K.KERNEL_AUTO, "simt": K.KERNEL_SIMT, "decode": K.KERNEL_DECODE,
+              "tc": K.KERNEL_TC}[args.kernel]
+    inp = wl.make_inputs(w, device=f"cuda:{dev}")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, device=f"cuda:{dev}", kernel=kernel)
+    out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
+    lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
+    acc = workload_accounting(w, inp.q_len, inp.kv_len, run.block_cost, run.part_rows)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        run.plan()
+        if ev is not None:
+            ev[0].record(stream)
+        run.partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        if ev is not None:
+            ev[1].record(stream)
+        run.merge(out, lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_nvsmi_id(torch, dev), os.path.join(ROOT, f".bench_clocks_{dctx.rank}.csv"))
+    sampler.start()
+    dctx.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    host0 = time.perf_counter()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    host_s = time.perf_counter() - host0
+    dctx.barrier()
+    clocks = sampler.stop()
+    try:
+        os.remove(sampler.path)
+    except OSError:
+        pass
+    local_s = t0.elapsed_time(t1) / 1e3
+    partial_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    t_max, units = aggregate(dctx, local_s, acc["kv_bytes"] * args.steps, device=f"cuda:{dev}")
+    ms_per_step = 1e3 * t_max / args.steps
+
+    # planner time alone (host), for the report
+    tp = time.perf_counter()
+    for _ in range(20):
+        K.splitkv_plan(K.splitkv_block_costs(run._q_len_np, run._kv_len_np, w.block_len, w.causal),
+                       w.n_shards)
+    planner_us = (time.perf_counter() - tp) / 20 * 1e6
+
+    # end to end: host inputs -> device, the path, result -> host, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, w, inp, run, dev, acc)
+
+    peaks, peak_src = load_peaks()
+    kname = K.KERNEL_NAMES[run.kernel_used()]
+    hbm_bound = (acc["flops"] / acc["partial_bytes"]) < 1e3 * peaks["bf16_tflops"] / peaks["hbm_gbs"]
+    if hbm_bound:
+        achieved = acc["partial_bytes"] / (partial_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    else:
+        achieved = acc["flops"] / (partial_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    roof.update({"traffic": traffic_for(kname, w.name), "kernel": f"partial_{kname}",
+                 "kernel_ms": partial_ms, "peak_source": peak_src,
+                 "algorithmic_per_launch": acc["partial_bytes"] if hbm_bound else acc["flops"]})
+
+    value = units / t_max / 1e9  # GB/s of K/V read, all ranks
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dctx.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "tflops": acc["flops"] * args.steps * dctx.world / t_max / 1e12,
+        "config": {"workload": w.name, "shape": w.description, "kernel": kname,
+                   "n_items": run.n_items, "lpt_imbalance": run.imbalance,
+                   "planner_us": planner_us, "host_s": host_s,
+                   "l2": f"inputs larger than L2 (K/V {acc['kv_bytes'] / 1e9:.2f} GB vs L2 "
+                         f"{L2_BYTES / 1e6:.0f} MB); no flush"
+                         if acc["kv_bytes"] > L2_BYTES else "inputs smaller than L2; not flushed",
+                   "parallelism": f"replicas x{dctx.world}"},
+        "roofline": roof,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if dctx.rank == 0 and dctx.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if dctx.rank == 0:
+        print(json.dumps(line), flush=True)
+    dctx.finish()
+
+
+def run_e2e(args, w, inp, run, dev, acc):
+    import torch
+
+    d = f"cuda:{dev}"
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("q", "k_pool", "v_pool", "block_table")}
+    dbuf = {k: torch.empty_like(v, device=d) for k, v in host.items()}
+    out_h = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype).pin_memory()
+    lse_h = torch.empty((run.total_q, w.Hq), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def one():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        out, lse = run(dbuf["q"], dbuf["k_pool"], dbuf["v_pool"], dbuf["block_table"], w.scale)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    n = args.e2e_steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    s = t0.elapsed_time(t1) / 1e3
+    h2d += run.work_host.size * 4
+    del dbuf
+    return {"value": acc["kv_bytes"] * n / s / 1e9, "unit": "GB/s", "ms_per_step": 1e3 * s / n,
+            "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------- oracle on the host
+
+
+def _oracle_unit(w, inp_cpu, b, kvh, n_keys=None):
+    """The oracle's unsharded attention for sequence b, K/V head kvh (its G query heads).
+
+    ``n_keys`` truncates the sequence to its first n_keys keys (a bounded sample;
+    the queries keep their place at the end of the truncated sequence)."""
+    import oracle
+
+    cu = int(sum(inp_cpu["q_len"][:b]))
+    lq = inp_cpu["q_len"][b]
+    g = w.G
+    kv = inp_cpu["kv_len"][b] if n_keys is None else max(lq, min(n_keys, inp_cpu["kv_len"][b]))
+    q = inp_cpu["q"][cu: cu + lq, kvh * g: (kvh + 1) * g]
+    kp = inp_cpu["k_pool"][:, :, kvh: kvh + 1]
+    vp = inp_cpu["v_pool"][:, :, kvh: kvh + 1]
+    table = inp_cpu["block_table"][b: b + 1]
+    oracle.attention(q, kp, vp, table, [lq], [kv], w.block_len, w.causal, w.scale)
+    return kv
+
+
+def _unit_bytes(w, n_keys):
+    return float(n_keys) * w.d * 2 * w.elem_bytes
+
+
+def cpu_baseline(w, inp, seconds):
+    """Times the fp64 oracle as it stands on the host cores over a bounded sample."""
+    import torch
+
+    torch.set_num_threads(os.cpu_count() or 1)
+    cpu = {"q": inp.q.cpu(), "k_pool": inp.k_pool.cpu(), "v_pool": inp.v_pool.cpu(),
+           "block_table": inp.block_table.cpu(), "q_len": inp.q_len, "kv_len": inp.kv_len}
+    units = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    t0 = time.perf_counter()
+    done, nbytes = 0, 0.0
+    for b, h in units:
+        nbytes += _unit_bytes(w, _oracle_unit(w, cpu, b, h))
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    s = time.perf_counter() - t0
+    return {"value": nbytes / s / 1e9, "unit": "GB/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "seconds": s,
+            "sample": f"{done} of {len(units)} (sequence, K/V head) units of the workload, "
+                      f"fp64 unsharded attention over their full context"}
+
+
+def run_reference(args, dctx):
+    """The oracle as the reference arm: rank 0 only, bounded sample per step."""
+    import torch
+
+    from context_long_attention_lpt_gb300 import workloads as wl
+
+    if dctx.rank != 0:
+        return
+    torch.set_num_threads(os.cpu_count() or 1)
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, device="cpu")
+    cpu = {"q": inp.q, "k_pool": inp.k_pool, "v_pool": inp.v_pool, "block_table": inp.block_table,
+           "q_len": inp.q_len, "kv_len": inp.kv_len}
+    units = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    # size each step (keys of one (sequence, K/V head) unit) so the whole run fits the budget
+    t0 = time.perf_counter()
+    full = _oracle_unit(w, cpu, *units[0])
+    per_key = (time.perf_counter() - t0) / full
+    budget = 150.0
+    n_keys = int(budget / (args.steps + args.warmup) / per_key)
+    n_keys = max(w.block_len, min(full, (n_keys // w.block_len) * w.block_len))
+    for i in range(args.warmup):
+        _oracle_unit(w, cpu, *units[i % len(units)], n_keys=n_keys)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for i in range(args.steps):
+        b, h = units[i % len(units)]
+        nbytes += _unit_bytes(w, _oracle_unit(w, cpu, b, h, n_keys=n_keys))
+    s = time.perf_counter() - t0
+    value = nbytes / s / 1e9
+    sample = (f"per step one (sequence, K/V head) unit of the workload truncated to its first {n_keys} "
+              f"keys, fp64 unsharded attention")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dctx.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "shape": w.description},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle",
+                             "cores": torch.get_num_threads(), "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dctx = Dist()
+    if args.impl == "reference":
+        run_reference(args, dctx)
+        return
+    run_ours(args, dctx)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+// extern "C" device-side entry points: argument validation, kernel choice, launch.
+
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "splitkv.h"
+#include "status.h"
+
+using splitkv::fail;
+
+namespace {
+
+// Bit 0: a block-table entry outside the pool was skipped.
+__device__ unsigned int g_device_status = 0;
+
+unsigned int* status_word(int* err) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+  if (e != cudaSuccess) {
+    *err = fail(SPLITKV_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    return nullptr;
+  }
+  return static_cast<unsigned int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pick_kernel(const splitkv::PartialArgs& a, int32_t requested) {
+  if (requested != SPLITKV_KERNEL_AUTO) return requested;
+  if (splitkv::tc_supports(a)) return SPLITKV_KERNEL_TC;
+  if (splitkv::decode_supports(a)) return SPLITKV_KERNEL_DECODE;
+  return SPLITKV_KERNEL_SIMT;
+}
+
+}  // namespace
+
+extern "C" int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len,
+                                   int32_t max_q_len, int32_t dtype) {
+  splitkv::PartialArgs a{};
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.block_len = block_len;
+  a.max_q_len = max_q_len;
+  a.dtype = dtype;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return fail(SPLITKV_ERR_INVALID, "bad head counts");
+  return pick_kernel(a, SPLITKV_KERNEL_AUTO);
+}
+
+extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
+                                    int64_t n_pool_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* work,
+                                    int32_t n_items, int32_t B, int32_t total_q,
+                                    int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t d,
+                                    int32_t block_len, float scale, int32_t causal,
+                                    int32_t dtype, float* o_part, float* lse_part,
+                                    int64_t part_rows, int32_t kernel, void* stream) {
+  if (dtype != SPLITKV_F32 && dtype != SPLITKV_BF16)
+    return fail(SPLITKV_ERR_INVALID, "dtype must be SPLITKV_F32 or SPLITKV_BF16 (got %d)", dtype);
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(SPLITKV_ERR_INVALID, "need B > 0 and Hq a positive multiple of Hkv (B=%d Hq=%d Hkv=%d)",
+                B, Hq, Hkv);
+  if (d != 64 && d != 128) return fail(SPLITKV_ERR_UNSUPPORTED, "head dim %d not supported (64, 128)", d);
+  if (block_len <= 0 || n_pool_blocks < 0 || max_blocks_per_seq < 0 || n_items < 0 || total_q < 0 ||
+      max_q_len < 0 || part_rows < 0)
+    return fail(SPLITKV_ERR_INVALID, "negative size argument");
+  if (!std::isfinite(scale)) return fail(SPLITKV_ERR_INVALID, "scale must be finite");
+  if (n_items > 0 && (!q || !k_pool || !v_pool || !block_table || !work || !o_part || !lse_part))
+    return fail(SPLITKV_ERR_INVALID, "null device pointer");
+  if (!work) return fail(SPLITKV_ERR_INVALID, "null work descriptor");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o_part))
+    return fail(SPLITKV_ERR_INVALID, "q, k_pool, v_pool and o_part must be 16-byte aligned");
+  if (kernel < SPLITKV_KERNEL_AUTO || kernel > SPLITKV_KERNEL_TC)
+    return fail(SPLITKV_ERR_INVALID, "unknown kernel %d", kernel);
+  int err = 0;
+  splitkv::PartialArgs a{q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work,
+                         n_items, B, total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal ? 1 : 0,
+                         dtype, o_part, lse_part, part_rows, nullptr};
+  a.status = status_word(&err);
+  if (!a.status) return err;
+  if (n_items == 0) {
+    splitkv::clear_error();
+    return SPLITKV_OK;
+  }
+  const int k = pick_kernel(a, kernel);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (k) {
+    case SPLITKV_KERNEL_TC:
+      if (!splitkv::tc_supports(a))
+        return fail(SPLITKV_ERR_UNSUPPORTED, "tensor-core kernel needs bf16, d=128, block_len %% 128 == 0, "
+                    "128 %% G == 0");
+      e = splitkv::launch_partial_tc(a, s);
+      break;
+    case SPLITKV_KERNEL_DECODE:
+      if (!splitkv::decode_supports(a))
+        return fail(SPLITKV_ERR_UNSUPPORTED, "decode kernel needs bf16, d=128 and q_len*G <= 16");
+      e = splitkv::launch_partial_decode(a, s);
+      break;
+    default:
+      e = splitkv::launch_partial_simt(a, s);
+      break;
+  }
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "partial launch: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int splitkv_merge(const float* o_part, const float* lse_part, int64_t part_rows,
+                             const int32_t* work, int32_t B, int32_t total_q, int32_t Hq, int32_t d,
+                             int32_t dtype, void* out, float* lse_out, void* stream) {
+  if (dtype != SPLITKV_F32 && dtype != SPLITKV_BF16)
+    return fail(SPLITKV_ERR_INVALID, "dtype must be SPLITKV_F32 or SPLITKV_BF16 (got %d)", dtype);
+  if (d != 64 && d != 128) return fail(SPLITKV_ERR_UNSUPPORTED, "head dim %d not supported (64, 128)", d);
+  if (B <= 0 || Hq <= 0 || total_q < 0) return fail(SPLITKV_ERR_INVALID, "bad sizes");
+  if (total_q > 0 && (!o_part || !lse_part || !work || !out || !lse_out))
+    return fail(SPLITKV_ERR_INVALID, "null device pointer");
+  if (!aligned16(o_part)) return fail(SPLITKV_ERR_INVALID, "o_part must be 16-byte aligned");
+  if (part_rows < 0) return fail(SPLITKV_ERR_INVALID, "negative part_rows");
+  int err = 0;
+  unsigned int* status = status_word(&err);
+  if (!status) return err;
+  const cudaError_t e = splitkv::launch_merge(o_part, lse_part, part_rows, work, B, total_q, Hq, d,
+                                              dtype, out, lse_out, status,
+                                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int splitkv_device_status(uint32_t* status, int32_t clear) {
+  if (!status) return fail(SPLITKV_ERR_INVALID, "null status pointer");
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
+  *status = v;
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}

@@ -1,0 +1,52 @@
+// Internal launch interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "splitkv.h"
+
+namespace splitkv {
+
+// Arguments of one partial-attention launch, already validated by the ABI layer.
+struct PartialArgs {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  int64_t n_pool_blocks;
+  const int32_t* block_table;
+  int32_t max_blocks_per_seq;
+  const int32_t* work;
+  int32_t n_items;
+  int32_t B;
+  int32_t total_q;
+  int32_t max_q_len;
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t d;
+  int32_t block_len;
+  float scale;
+  int32_t causal;
+  int32_t dtype;
+  float* o_part;
+  float* lse_part;
+  int64_t part_rows;
+  unsigned int* status;  // device status word (bit 0: block-table entry out of range)
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);
+cudaError_t launch_partial_decode(const PartialArgs& a, cudaStream_t stream);
+cudaError_t launch_partial_tc(const PartialArgs& a, cudaStream_t stream);
+
+// Shape limits of the specialised kernels (checked before launching them).
+bool decode_supports(const PartialArgs& a);
+bool tc_supports(const PartialArgs& a);
+
+cudaError_t launch_merge(const float* o_part, const float* lse_part, int64_t part_rows,
+                         const int32_t* work, int32_t B, int32_t total_q, int32_t Hq, int32_t d,
+                         int32_t dtype, void* out, float* lse_out, unsigned int* status,
+                         cudaStream_t stream);
+
+}  // namespace splitkv

@@ -1,0 +1,279 @@
+// Host side of the split-KV path: block costing, LPT allocation, work lists.
+//
+// Follows the Split-KV knowledge card (kongchang.com), "Timeline" and "All
+// Facts": context KV blocks go to the CP shards by a cost-aware
+// longest-processing-time-first rule.  The card leaves the cost and the tie
+// order open; this file takes cost = visible (query, key) pairs of a block,
+// ties by lower global block index and then lower shard id.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "splitkv.h"
+#include "status.h"
+#include "work_layout.h"
+
+using splitkv::fail;
+
+namespace {
+
+// Visible (query, key) pairs of keys [lo, hi) for q_len queries whose token t
+// sees keys [0, a0 + t) (causal tail) - the sum over t of clamp(a0+t-lo, 0, hi-lo),
+// in closed form: the terms are 0, then rise by one per query, then saturate.
+int64_t causal_pairs(int64_t q_len, int64_t a0, int64_t lo, int64_t hi) {
+  const int64_t w = hi - lo;
+  const int64_t a = a0 - lo;  // term of query 0 before clamping
+  auto clampi = [](int64_t x, int64_t l, int64_t h) { return x < l ? l : (x > h ? h : x); };
+  const int64_t t_rise = clampi(-a + 1, 0, q_len);  // queries whose term is <= 0
+  const int64_t t_sat = clampi(w - a, 0, q_len);    // first query whose term is >= w
+  int64_t total = (q_len - t_sat) * w;
+  if (t_sat > t_rise) {
+    const int64_t n = t_sat - t_rise;
+    total += n * a + (t_sat * (t_sat - 1) - t_rise * (t_rise - 1)) / 2;
+  }
+  return total;
+}
+
+bool check_lengths(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
+                   int* status) {
+  if (!q_len || !kv_len) { *status = fail(SPLITKV_ERR_INVALID, "null length array"); return false; }
+  if (B <= 0) { *status = fail(SPLITKV_ERR_INVALID, "B must be positive (got %d)", B); return false; }
+  if (block_len <= 0) {
+    *status = fail(SPLITKV_ERR_INVALID, "block_len must be positive (got %d)", block_len);
+    return false;
+  }
+  for (int32_t b = 0; b < B; ++b) {
+    if (q_len[b] < 0 || kv_len[b] < 0 || q_len[b] > kv_len[b]) {
+      *status = fail(SPLITKV_ERR_INVALID,
+                     "sequence %d: need 0 <= q_len (%d) <= kv_len (%d)", b, q_len[b], kv_len[b]);
+      return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" int64_t splitkv_num_blocks(const int32_t* kv_len, int32_t B, int32_t block_len) {
+  if (!kv_len || B <= 0 || block_len <= 0)
+    return fail(SPLITKV_ERR_INVALID, "splitkv_num_blocks: bad arguments");
+  int64_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (kv_len[b] < 0) return fail(SPLITKV_ERR_INVALID, "negative kv_len");
+    n += (static_cast<int64_t>(kv_len[b]) + block_len - 1) / block_len;
+  }
+  splitkv::clear_error();
+  return n;
+}
+
+extern "C" int splitkv_block_costs(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                                   int32_t block_len, int32_t causal, int64_t* block_cost,
+                                   int64_t n_blocks) {
+  int st = 0;
+  if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
+  if (!block_cost) return fail(SPLITKV_ERR_INVALID, "null block_cost");
+  int64_t g = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t lq = q_len[b], lk = kv_len[b];
+    const int64_t nb = (lk + block_len - 1) / block_len;
+    if (g + nb > n_blocks)
+      return fail(SPLITKV_ERR_CAPACITY, "block_cost holds %lld blocks, batch has more",
+                  (long long)n_blocks);
+    for (int64_t j = 0; j < nb; ++j) {
+      const int64_t lo = j * block_len;
+      const int64_t hi = std::min<int64_t>(lk, lo + block_len);
+      block_cost[g++] = causal ? causal_pairs(lq, lk - lq + 1, lo, hi) : lq * (hi - lo);
+    }
+  }
+  if (g != n_blocks)
+    return fail(SPLITKV_ERR_INVALID, "n_blocks = %lld but the batch has %lld blocks",
+                (long long)n_blocks, (long long)g);
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t n_shards,
+                            int32_t* shard_of_block, int64_t* shard_load) {
+  if (n_blocks < 0 || (n_blocks > 0 && (!block_cost || !shard_of_block)))
+    return fail(SPLITKV_ERR_INVALID, "splitkv_plan: bad block arrays");
+  if (n_shards <= 0 || !shard_load)
+    return fail(SPLITKV_ERR_INVALID, "splitkv_plan: n_shards must be positive (got %d)", n_shards);
+  for (int64_t g = 0; g < n_blocks; ++g)
+    if (block_cost[g] < 0) return fail(SPLITKV_ERR_INVALID, "negative cost at block %lld", (long long)g);
+
+  // Longest first; equal costs keep ascending block index.
+  std::vector<int64_t> order(static_cast<size_t>(n_blocks));
+  for (int64_t g = 0; g < n_blocks; ++g) order[g] = g;
+  std::sort(order.begin(), order.end(), [&](int64_t x, int64_t y) {
+    return block_cost[x] != block_cost[y] ? block_cost[x] > block_cost[y] : x < y;
+  });
+
+  // Least-loaded shard = smallest (load, id): a min-heap on that pair.
+  using Slot = std::pair<int64_t, int32_t>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int32_t s = 0; s < n_shards; ++s) heap.push({0, s});
+  for (int64_t g : order) {
+    Slot top = heap.top();
+    heap.pop();
+    shard_of_block[g] = top.second;
+    top.first += block_cost[g];
+    heap.push(top);
+  }
+  for (int32_t s = 0; s < n_shards; ++s) shard_load[s] = 0;
+  while (!heap.empty()) {
+    shard_load[heap.top().second] = heap.top().first;
+    heap.pop();
+  }
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int64_t splitkv_work_words(int64_t n_blocks, int32_t B) {
+  if (n_blocks < 0 || B <= 0) return fail(SPLITKV_ERR_INVALID, "splitkv_work_words: bad arguments");
+  return splitkv::kHeaderWords + splitkv::kSeqWords * (static_cast<int64_t>(B) + 1) +
+         (splitkv::kItemWords + 2) * n_blocks;
+}
+
+extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                                  int32_t block_len, const int64_t* block_cost,
+                                  const int32_t* shard_of_block, int64_t n_blocks,
+                                  int32_t n_shards, int32_t* work, int64_t work_words,
+                                  int32_t* n_items_out, int64_t* part_rows_out) {
+  using namespace splitkv;
+  int st = 0;
+  if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
+  if (!work || !n_items_out || !part_rows_out || (n_blocks > 0 && (!block_cost || !shard_of_block)))
+    return fail(SPLITKV_ERR_INVALID, "splitkv_build_work: null argument");
+  if (n_shards <= 0) return fail(SPLITKV_ERR_INVALID, "n_shards must be positive");
+  const int64_t need = splitkv_work_words(n_blocks, B);
+  if (need < 0) return static_cast<int>(need);
+  if (work_words < need)
+    return fail(SPLITKV_ERR_CAPACITY, "work buffer holds %lld words, needs %lld",
+                (long long)work_words, (long long)need);
+
+  // Global block g -> (sequence, logical block).
+  std::vector<int32_t> seq_of(static_cast<size_t>(n_blocks)), blk_of(static_cast<size_t>(n_blocks));
+  int64_t g = 0;
+  int64_t total_q = 0;
+  int32_t max_q = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t nb = (static_cast<int64_t>(kv_len[b]) + block_len - 1) / block_len;
+    if (g + nb > n_blocks) return fail(SPLITKV_ERR_INVALID, "n_blocks is smaller than the batch");
+    for (int64_t j = 0; j < nb; ++j, ++g) {
+      seq_of[g] = b;
+      blk_of[g] = static_cast<int32_t>(j);
+    }
+    total_q += q_len[b];
+    max_q = std::max(max_q, q_len[b]);
+  }
+  if (g != n_blocks) return fail(SPLITKV_ERR_INVALID, "n_blocks does not match kv_len/block_len");
+  if (total_q > INT32_MAX) return fail(SPLITKV_ERR_UNSUPPORTED, "total_q exceeds int32");
+  for (int64_t i = 0; i < n_blocks; ++i)
+    if (shard_of_block[i] < 0 || shard_of_block[i] >= n_shards)
+      return fail(SPLITKV_ERR_INVALID, "shard_of_block[%lld] = %d out of range", (long long)i,
+                  shard_of_block[i]);
+
+  // Group blocks by (shard, sequence); within a group blocks stay ascending.
+  std::vector<int64_t> idx(static_cast<size_t>(n_blocks));
+  for (int64_t i = 0; i < n_blocks; ++i) idx[i] = i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int64_t x, int64_t y) {
+    if (shard_of_block[x] != shard_of_block[y]) return shard_of_block[x] < shard_of_block[y];
+    return seq_of[x] < seq_of[y];
+  });
+  struct Item {
+    int32_t shard, seq;
+    int64_t first, count, cost;
+  };
+  std::vector<Item> items;
+  for (int64_t i = 0; i < n_blocks;) {
+    int64_t j = i;
+    Item it{shard_of_block[idx[i]], seq_of[idx[i]], i, 0, 0};
+    while (j < n_blocks && shard_of_block[idx[j]] == it.shard && seq_of[idx[j]] == it.seq) {
+      it.cost += block_cost[idx[j]];
+      ++j;
+    }
+    it.count = j - i;
+    items.push_back(it);
+    i = j;
+  }
+  // Launch order: largest item first, then shard, then sequence.
+  std::vector<int32_t> order(items.size());
+  for (size_t i = 0; i < items.size(); ++i) order[i] = static_cast<int32_t>(i);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+    return items[x].cost > items[y].cost;
+  });
+
+  const int32_t n_items = static_cast<int32_t>(items.size());
+  const int64_t off_seq = kHeaderWords;
+  const int64_t off_items = off_seq + kSeqWords * (static_cast<int64_t>(B) + 1);
+  const int64_t off_blocks = off_items + kItemWords * static_cast<int64_t>(n_items);
+  const int64_t off_seq_items = off_blocks + n_blocks;
+  std::memset(work, 0, sizeof(int32_t) * static_cast<size_t>(off_seq_items + n_items));
+
+  int32_t* hdr = work;
+  hdr[kMagic] = kWorkMagic;
+  hdr[kB] = B;
+  hdr[kNItems] = n_items;
+  hdr[kNShards] = n_shards;
+  hdr[kBlockLen] = block_len;
+  hdr[kTotalQ] = static_cast<int32_t>(total_q);
+  hdr[kMaxQ] = max_q;
+  hdr[kOffSeq] = static_cast<int32_t>(off_seq);
+  hdr[kOffItems] = static_cast<int32_t>(off_items);
+  hdr[kOffBlocks] = static_cast<int32_t>(off_blocks);
+  hdr[kOffSeqItems] = static_cast<int32_t>(off_seq_items);
+  hdr[kNBlocks] = static_cast<int32_t>(n_blocks);
+  if (off_seq_items + n_items > INT32_MAX) return fail(SPLITKV_ERR_UNSUPPORTED, "work descriptor too large");
+
+  int64_t part_row = 0;
+  int64_t blk_cursor = 0;
+  std::vector<int32_t> rank_of(items.size());
+  for (int32_t r = 0; r < n_items; ++r) {
+    const Item& it = items[order[r]];
+    rank_of[order[r]] = r;
+    int32_t* w = work + off_items + kItemWords * static_cast<int64_t>(r);
+    w[kItShard] = it.shard;
+    w[kItSeq] = it.seq;
+    w[kItBlockOff] = static_cast<int32_t>(blk_cursor);
+    w[kItBlockCnt] = static_cast<int32_t>(it.count);
+    if (part_row > INT32_MAX) return fail(SPLITKV_ERR_UNSUPPORTED, "partial rows exceed int32");
+    w[kItPartRow] = static_cast<int32_t>(part_row);
+    w[kItCostLo] = static_cast<int32_t>(static_cast<uint64_t>(it.cost) & 0xffffffffu);
+    w[kItCostHi] = static_cast<int32_t>(static_cast<uint64_t>(it.cost) >> 32);
+    for (int64_t k = 0; k < it.count; ++k) work[off_blocks + blk_cursor + k] = blk_of[idx[it.first + k]];
+    blk_cursor += it.count;
+    part_row += q_len[it.seq];
+  }
+  // Per sequence: its items, ascending shard (items were built shard-major).
+  std::vector<int32_t> per_seq_count(B, 0);
+  for (const Item& it : items) per_seq_count[it.seq]++;
+  int32_t ptr = 0;
+  int64_t cu = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t* s = work + off_seq + kSeqWords * b;
+    s[0] = static_cast<int32_t>(cu);
+    s[1] = q_len[b];
+    s[2] = kv_len[b];
+    s[3] = ptr;
+    ptr += per_seq_count[b];
+    cu += q_len[b];
+  }
+  int32_t* last = work + off_seq + kSeqWords * B;
+  last[0] = static_cast<int32_t>(total_q);
+  last[3] = n_items;
+  std::vector<int32_t> fill(B, 0);
+  for (size_t i = 0; i < items.size(); ++i) {
+    const int32_t b = items[i].seq;
+    const int32_t base = work[off_seq + kSeqWords * b + 3];
+    work[off_seq_items + base + fill[b]++] = rank_of[i];
+  }
+  *n_items_out = n_items;
+  *part_rows_out = part_row;
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}

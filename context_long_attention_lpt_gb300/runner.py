@@ -1,0 +1,111 @@
+"""One split-KV attention pass through the C ABI, for a batch of sequences.
+
+``SplitKVAttention`` strings the library calls together in the path's order:
+
+    splitkv_block_costs -> splitkv_plan -> splitkv_build_work   (host)
+    copy work descriptor to the device
+    splitkv_attn_partial -> splitkv_merge                        (device, one stream)
+
+It owns the device buffers the calls need (work descriptor, partials, outputs),
+allocated with torch and reused across calls of the same shape.  It computes
+nothing itself.
+"""
+
+import numpy as np
+import torch
+
+from . import splitkv as _k
+
+
+class SplitKVAttention:
+    def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
+                 device="cuda", kernel=_k.KERNEL_AUTO):
+        self.q_len = [int(x) for x in q_len]
+        self.kv_len = [int(x) for x in kv_len]
+        self.B = len(self.q_len)
+        self.block_len = int(block_len)
+        self.causal = bool(causal)
+        self.n_shards = int(n_shards)
+        self.Hq, self.Hkv, self.d = int(Hq), int(Hkv), int(d)
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.kernel = kernel
+        self.total_q = sum(self.q_len)
+        self.max_q_len = max(self.q_len) if self.q_len else 0
+        self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
+        self._kv_len_np = np.asarray(self.kv_len, dtype=np.int32)
+        self._work_host = None
+        self._work_dev = None
+        self._work_copied = None
+        self._o_part = None
+        self._lse_part = None
+        self.plan()
+
+    # host steps -------------------------------------------------------------
+    def plan(self):
+        """Block costs, LPT plan and work lists on the host; copy the work to the device."""
+        self.block_cost = _k.splitkv_block_costs(self._q_len_np, self._kv_len_np, self.block_len,
+                                                 self.causal)
+        self.shard_of_block, self.shard_load = _k.splitkv_plan(self.block_cost, self.n_shards)
+        work, self.n_items, self.part_rows = _k.splitkv_build_work(
+            self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
+            self.n_shards)
+        if self._work_copied is not None:
+            self._work_copied.synchronize()  # the previous upload has left the pinned buffer
+        if self._work_host is None or self._work_host.numel() < work.size:
+            self._work_host = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
+            self._work_dev = torch.empty(work.size, dtype=torch.int32, device=self.device)
+        self._work_host[: work.size].copy_(torch.from_numpy(work))
+        self._work_dev[: work.size].copy_(self._work_host[: work.size], non_blocking=True)
+        self._work_copied = torch.cuda.Event()
+        self._work_copied.record()
+        self.work_host = work
+        if self._o_part is None or self._o_part.shape[0] < self.part_rows:
+            self._o_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32,
+                                       device=self.device)
+            self._lse_part = torch.empty((max(self.part_rows, 1), self.Hq), dtype=torch.float32,
+                                         device=self.device)
+        return self
+
+    @property
+    def imbalance(self):
+        load = self.shard_load
+        mean = load.sum() / len(load)
+        return float(load.max() / mean - 1.0) if mean > 0 else 0.0
+
+    @property
+    def o_part(self):
+        return self._o_part[: self.part_rows]
+
+    @property
+    def lse_part(self):
+        return self._lse_part[: self.part_rows]
+
+    @property
+    def work_device(self):
+        return self._work_dev
+
+    def kernel_used(self):
+        if self.kernel != _k.KERNEL_AUTO:
+            return self.kernel
+        code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
+        return _k.splitkv_auto_kernel(self.Hq, self.Hkv, self.d, self.block_len, self.max_q_len, code)
+
+    # device steps -----------------------------------------------------------
+    def partial(self, q, k_pool, v_pool, block_table, scale, stream=None):
+        _k.splitkv_attn_partial(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+                                self.total_q, self.max_q_len, self.block_len, scale, self.causal,
+                                self._o_part, self._lse_part, kernel=self.kernel, stream=stream)
+
+    def merge(self, out, lse, stream=None):
+        _k.splitkv_merge(self._o_part, self._lse_part, self._work_dev, self.B, self.total_q, out, lse,
+                         stream=stream)
+
+    def __call__(self, q, k_pool, v_pool, block_table, scale, out=None, lse=None, stream=None):
+        if out is None:
+            out = torch.empty((self.total_q, self.Hq, self.d), dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty((self.total_q, self.Hq), dtype=torch.float32, device=q.device)
+        self.partial(q, k_pool, v_pool, block_table, scale, stream=stream)
+        self.merge(out, lse, stream=stream)
+        return out, lse

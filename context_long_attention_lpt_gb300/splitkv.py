@@ -1,0 +1,190 @@
+"""Python binding of libsplitkv.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+include/splitkv.h) and does nothing but turn numpy arrays / torch tensors into
+pointers and sizes, call the library, and raise on a negative status.  All
+arithmetic of the path - block costs, the LPT plan, the work lists, partial
+attention, the merge - runs in the library.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsplitkv.so")
+_lib = None
+
+SPLITKV_F32 = 0
+SPLITKV_BF16 = 1
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_DECODE, KERNEL_TC = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_SIMT: "simt", KERNEL_DECODE: "decode", KERNEL_TC: "tcgen05"}
+
+_i32, _i64, _f32, _p, _u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_uint32
+
+_SIGNATURES = {
+    "splitkv_num_blocks": (_i64, [_p, _i32, _i32]),
+    "splitkv_block_costs": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _i64]),
+    "splitkv_plan": (ctypes.c_int, [_p, _i64, _i32, _p, _p]),
+    "splitkv_work_words": (_i64, [_i64, _i32]),
+    "splitkv_build_work": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _p, _i64, _p, _p]),
+    "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "splitkv_attn_partial": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                             _i32, _i32, _i32, _i32, _f32, _i32, _i32, _p, _p, _i64,
+                                             _i32, _p]),
+    "splitkv_merge": (ctypes.c_int, [_p, _p, _i64, _p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]),
+    "splitkv_device_status": (ctypes.c_int, [_p, _i32]),
+    "splitkv_last_error": (ctypes.c_char_p, []),
+}
+
+
+class SplitKVError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded library (loaded on first use; raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libsplitkv.so not found at {_LIB_PATH}; build it first "
+                "(python -m context_long_attention_lpt_gb300.build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def splitkv_last_error():
+    return lib().splitkv_last_error().decode()
+
+
+def _check(fn, status):
+    if status < 0:
+        raise SplitKVError(fn, status, splitkv_last_error())
+    return status
+
+
+def _np(a, dtype):
+    return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------ host calls
+
+
+def splitkv_num_blocks(kv_len, block_len):
+    kv = _np(kv_len, np.int32)
+    return _check("splitkv_num_blocks", lib().splitkv_num_blocks(_ptr(kv), len(kv), block_len))
+
+
+def splitkv_block_costs(q_len, kv_len, block_len, causal):
+    q, kv = _np(q_len, np.int32), _np(kv_len, np.int32)
+    n = splitkv_num_blocks(kv, block_len)
+    out = np.zeros(n, dtype=np.int64)
+    _check("splitkv_block_costs", lib().splitkv_block_costs(_ptr(q), _ptr(kv), len(q), block_len,
+                                                           int(bool(causal)), _ptr(out), n))
+    return out
+
+
+def splitkv_plan(block_cost, n_shards):
+    c = _np(block_cost, np.int64)
+    sob = np.zeros(len(c), dtype=np.int32)
+    load = np.zeros(n_shards, dtype=np.int64)
+    _check("splitkv_plan", lib().splitkv_plan(_ptr(c), len(c), n_shards, _ptr(sob), _ptr(load)))
+    return sob, load
+
+
+def splitkv_work_words(n_blocks, B):
+    return _check("splitkv_work_words", lib().splitkv_work_words(n_blocks, B))
+
+
+def splitkv_build_work(q_len, kv_len, block_len, block_cost, shard_of_block, n_shards):
+    """Returns (work int32 array, n_items, part_rows)."""
+    q, kv = _np(q_len, np.int32), _np(kv_len, np.int32)
+    c, sob = _np(block_cost, np.int64), _np(shard_of_block, np.int32)
+    words = splitkv_work_words(len(c), len(q))
+    work = np.zeros(words, dtype=np.int32)
+    n_items = ctypes.c_int32(0)
+    part_rows = ctypes.c_int64(0)
+    _check("splitkv_build_work",
+           lib().splitkv_build_work(_ptr(q), _ptr(kv), len(q), block_len, _ptr(c), _ptr(sob), len(c),
+                                    n_shards, _ptr(work), words, ctypes.byref(n_items),
+                                    ctypes.byref(part_rows)))
+    return work, n_items.value, part_rows.value
+
+
+def splitkv_auto_kernel(Hq, Hkv, d, block_len, max_q_len, dtype):
+    return _check("splitkv_auto_kernel", lib().splitkv_auto_kernel(Hq, Hkv, d, block_len, max_q_len, dtype))
+
+
+# ---------------------------------------------------------------- device calls
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return SPLITKV_F32
+    if t.dtype == torch.bfloat16:
+        return SPLITKV_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def splitkv_attn_partial(q, k_pool, v_pool, block_table, work, n_items, B, total_q, max_q_len,
+                         block_len, scale, causal, o_part, lse_part, kernel=KERNEL_AUTO, stream=None):
+    """q [total_q, Hq, d], k_pool/v_pool [n_pool, block_len, Hkv, d], block_table int32 [B, max_blk],
+    work int32 (device), o_part fp32 [part_rows, Hq, d], lse_part fp32 [part_rows, Hq]."""
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
+                    ("work", work), ("o_part", o_part), ("lse_part", lse_part)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _, hq, d = q.shape
+    n_pool, bl, hkv, d2 = k_pool.shape
+    if d2 != d or bl != block_len:
+        raise ValueError("k_pool shape does not match q / block_len")
+    _check("splitkv_attn_partial", lib().splitkv_attn_partial(
+        q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), n_pool, block_table.data_ptr(),
+        block_table.shape[1], work.data_ptr(), n_items, B, total_q, max_q_len, hq, hkv, d, block_len,
+        float(scale), int(bool(causal)), _dtype_code(q), o_part.data_ptr(), lse_part.data_ptr(),
+        o_part.shape[0], kernel, _stream_handle(stream)))
+
+
+def splitkv_merge(o_part, lse_part, work, B, total_q, out, lse_out, stream=None):
+    """out [total_q, Hq, d] (bf16 or fp32), lse_out fp32 [total_q, Hq]."""
+    _, hq, d = out.shape
+    _check("splitkv_merge", lib().splitkv_merge(
+        o_part.data_ptr(), lse_part.data_ptr(), o_part.shape[0], work.data_ptr(), B, total_q, hq, d,
+        _dtype_code(out),
+        out.data_ptr(), lse_out.data_ptr(), _stream_handle(stream)))
+
+
+def splitkv_device_status(clear=False):
+    v = ctypes.c_uint32(0)
+    _check("splitkv_device_status", lib().splitkv_device_status(ctypes.byref(v), int(bool(clear))))
+    return v.value

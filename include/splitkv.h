@@ -1,0 +1,163 @@
+/*
+ * splitkv.h - C ABI of the split-KV attention library (libsplitkv.so).
+ *
+ * Exact split-KV attention for very short queries against very long contexts,
+ * after the "Split-KV" knowledge card (kongchang.com):
+ *   - intro / "Timeline": K/V shards stay local to their device and each layer's
+ *     attention exchanges only tensors the size of the queries;
+ *   - "Timeline" / "All Facts": context KV blocks are allocated to the shards by
+ *     a cost-aware longest-processing-time-first (LPT) rule, load imbalance < 1%;
+ *   - "All Facts": the result is exact, strictly equal to the unsharded one.
+ * Here the shards are emulated as KV splits on one GPU.  The path is:
+ *   splitkv_block_costs -> splitkv_plan -> splitkv_build_work   (host, C++)
+ *   splitkv_attn_partial -> splitkv_merge                        (device, CUDA)
+ *
+ * Conventions shared by every call
+ *   - Query tensor q: [total_q, Hq, d], sequences concatenated; sequence b owns
+ *     rows cu_q[b] .. cu_q[b]+q_len[b]-1 (cu_q = prefix sum of q_len).
+ *   - K/V pools: [n_pool_blocks, block_len, Hkv, d], row-major; a sequence's
+ *     logical block j lives in physical block block_table[b*max_blocks_per_seq+j].
+ *   - GQA: query head h reads K/V head h / (Hq/Hkv).
+ *   - Query token t of sequence b sits at key position kv_len[b]-q_len[b]+t
+ *     (queries appended after the context).  causal != 0: key j is visible iff
+ *     j <= that position; causal == 0: all kv_len[b] keys are visible.
+ *   - Scores are scale * q.k; LSE values are natural-log log-sum-exp of the
+ *     visible scaled scores, -inf where nothing is visible.
+ *   - dtype: SPLITKV_F32 (fp32 Q/K/V, fp32 arithmetic) or SPLITKV_BF16 (bf16
+ *     Q/K/V, fp32 accumulation).
+ *   - Ownership: the caller owns every buffer.  Host calls take host pointers;
+ *     device calls take device pointers and a cudaStream_t passed as void*.
+ *     No call allocates device memory.  Device calls are asynchronous on the
+ *     stream and never synchronise.
+ *   - Errors: every call returns 0 (SPLITKV_OK) or a negative status, never
+ *     aborts; splitkv_last_error() gives a message for the calling thread.
+ *     Arguments are validated on the host before any launch.
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPLITKV_OK 0
+#define SPLITKV_ERR_INVALID (-1)     /* bad pointer, size or argument */
+#define SPLITKV_ERR_UNSUPPORTED (-2) /* shape the chosen kernel cannot run */
+#define SPLITKV_ERR_CUDA (-3)        /* a CUDA runtime / driver call failed */
+#define SPLITKV_ERR_CAPACITY (-4)    /* an output buffer is too small */
+
+#define SPLITKV_F32 0
+#define SPLITKV_BF16 1
+
+/* kernel choice for splitkv_attn_partial */
+#define SPLITKV_KERNEL_AUTO 0   /* pick the fastest kernel that supports the shape */
+#define SPLITKV_KERNEL_SIMT 1   /* generic CUDA-core kernel: any shape, fp32 or bf16 */
+#define SPLITKV_KERNEL_DECODE 2 /* CUDA-core decode kernel: bf16, d=128, q_len*G <= 16 */
+#define SPLITKV_KERNEL_TC 3     /* TMA + tcgen05/TMEM kernel: bf16, d=128, block_len%128==0 */
+
+/* ---------------------------------------------------------------- host side */
+
+/* Number of KV blocks of the batch: sum over b of ceil(kv_len[b] / block_len).
+ * Returns the count (>= 0) or a negative status. */
+int64_t splitkv_num_blocks(const int32_t* kv_len, int32_t B, int32_t block_len);
+
+/* Step 1, block costing ("cost-aware" LPT, Split-KV card, "Timeline").
+ * block_cost[g] (out, host, n_blocks entries) = number of (query, key) pairs of
+ * global block g left visible by the mask.  Blocks are numbered sequence after
+ * sequence, logical block order within a sequence.  A fully visible block costs
+ * q_len * tokens; a block holding a causal tail counts the triangle.
+ * q_len, kv_len: host [B].  n_blocks must equal splitkv_num_blocks(). */
+int splitkv_block_costs(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                        int32_t block_len, int32_t causal, int64_t* block_cost,
+                        int64_t n_blocks);
+
+/* Step 2, LPT allocation (Split-KV card, "Timeline" / "All Facts").
+ * Blocks are taken by cost, largest first (equal costs: lower global index
+ * first); each goes to the shard with the smallest load so far (equal loads:
+ * lower shard id).  Out (host): shard_of_block[n_blocks] in [0, n_shards),
+ * shard_load[n_shards] = summed cost per shard.  Integer only: bit-exact. */
+int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t n_shards,
+                 int32_t* shard_of_block, int64_t* shard_load);
+
+/* Upper bound, in int32 words, of the work descriptor built below. */
+int64_t splitkv_work_words(int64_t n_blocks, int32_t B);
+
+/* Step 2b, work lists.  Groups the plan into work items, one per (shard,
+ * sequence) pair that holds at least one block, and writes the int32 work
+ * descriptor consumed by splitkv_attn_partial / splitkv_merge (host buffer of
+ * work_words words; the caller copies it to the device).  Layout:
+ *   [0..15]  header: magic 0x534B5631, B, n_items, n_shards, block_len,
+ *            total_q, max_q_len, off_seq, off_items, off_blocks, off_seq_items,
+ *            n_blocks, 0...
+ *   off_seq        (B+1) x 4: {cu_q[b], q_len[b], kv_len[b], seq_item_ptr[b]};
+ *                  row B = {total_q, 0, 0, n_items}
+ *   off_items      n_items x 8: {shard, seq, block_off, block_cnt, part_row,
+ *                  cost_lo, cost_hi, 0}; items sorted by cost (largest first,
+ *                  then shard, then sequence) - the launch order
+ *   off_blocks     n_blocks: logical block indices, grouped by item, ascending
+ *   off_seq_items  n_items: item indices grouped by sequence, ascending shard
+ * Item i's partial output occupies rows part_row .. part_row+q_len[seq]-1 of
+ * the partial buffers; *part_rows (out) is the total row count (sum over items
+ * of q_len of its sequence) and *n_items (out) the number of items. */
+int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                       int32_t block_len, const int64_t* block_cost,
+                       const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+                       int32_t* work, int64_t work_words, int32_t* n_items,
+                       int64_t* part_rows);
+
+/* Which kernel SPLITKV_KERNEL_AUTO picks for a shape (a SPLITKV_KERNEL_* value). */
+int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len,
+                        int32_t max_q_len, int32_t dtype);
+
+/* -------------------------------------------------------------- device side */
+
+/* Step 3, per-shard partial attention (Split-KV card, intro / "Timeline": each
+ * shard attends only over its local KV blocks and emits a query-sized partial).
+ * For every work item (shard s, sequence b), every query token t of b and every
+ * query head h:
+ *     m = max_j s_j,  l = sum_j exp(s_j - m),
+ *     o_part[part_row+t, h, :] = sum_j exp(s_j - m) v_j / l,
+ *     lse_part[part_row+t, h]  = m + ln l          (-inf, o = 0 if none visible)
+ * over the keys j of s's blocks of b that token t sees; s_j = scale * q.k_j.
+ * In (device): q, k_pool, v_pool (dtype), block_table int32 [B, max_blocks_per_seq],
+ * work (the descriptor above, copied to the device).  Out (device, fp32):
+ * o_part [part_rows, Hq, d], lse_part [part_rows, Hq].  n_items, B, total_q,
+ * max_q_len and part_rows must match the descriptor.  kernel: SPLITKV_KERNEL_*.
+ * A block-table entry outside [0, n_pool_blocks) is not read: the block is
+ * skipped and bit 0 of the device status word is set (splitkv_device_status). */
+int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
+                         int64_t n_pool_blocks, const int32_t* block_table,
+                         int32_t max_blocks_per_seq, const int32_t* work, int32_t n_items,
+                         int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,
+                         int32_t Hkv, int32_t d, int32_t block_len, float scale,
+                         int32_t causal, int32_t dtype, float* o_part, float* lse_part,
+                         int64_t part_rows, int32_t kernel, void* stream);
+
+/* Step 4, exact merge of the partials (Split-KV card, "All Facts": identical to
+ * the unsharded result).  For every query row r of sequence b and head h, over
+ * the items i of b:  L = ln sum_i exp(L_i),  O = sum_i exp(L_i - L) O_i;
+ * items with L_i = -inf carry weight 0.  Only query-sized tensors are read.
+ * In (device): o_part, lse_part as written by splitkv_attn_partial (part_rows
+ * rows), work.  A partial row outside part_rows is not read (bit 1 of the
+ * device status word is set).
+ * Out (device): out [total_q, Hq, d] in dtype, lse_out fp32 [total_q, Hq]. */
+int splitkv_merge(const float* o_part, const float* lse_part, int64_t part_rows,
+                  const int32_t* work, int32_t B, int32_t total_q, int32_t Hq, int32_t d,
+                  int32_t dtype, void* out, float* lse_out, void* stream);
+
+/* Reads and optionally clears the device status word: bit 0, a logical block
+ * past max_blocks_per_seq or a block-table entry outside the pool was skipped;
+ * bit 1, a work item's partial rows fell outside part_rows (item skipped).
+ * Synchronises the device. */
+int splitkv_device_status(uint32_t* status, int32_t clear);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* splitkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_H */

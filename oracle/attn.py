@@ -132,9 +132,9 @@ def attention_rows(q, k_pool, v_pool, block_table, q_len, kv_len, block_len, cau
         lq, lk = int(q_len[b]), int(kv_len[b])
         key = (b, h // g)
         if key not in cache:
-            cache.clear()
-            k_seq = gather_sequence(k_pool, block_table[b], lk, block_len)[:, h // g]
-            v_seq = gather_sequence(v_pool, block_table[b], lk, block_len)[:, h // g]
+            cache.clear()  # one (sequence, K/V head) at a time keeps host memory small
+            k_seq = gather_sequence(k_pool[:, :, h // g], block_table[b], lk, block_len)
+            v_seq = gather_sequence(v_pool[:, :, h // g], block_table[b], lk, block_len)
             cache[key] = (k_seq, v_seq)
         k_seq, v_seq = cache[key]
         n_vis = visible_keys(lq, lk, t, causal)

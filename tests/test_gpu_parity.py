@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small cases compare every output element; the full-size workloads compare
+sampled rows the oracle computes one by one.  Every case poisons the K/V slots
+past each sequence's end with NaN, so a kernel that reads them fails.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_long_attention_lpt_gb300 import splitkv as K
+from context_long_attention_lpt_gb300 import workloads as wl
+from context_long_attention_lpt_gb300.runner import SplitKVAttention
+from tests.parity_helpers import (TOL_L, TOL_O, assert_close, compare_rows, full_reference,
+                                  max_errors, run_cuda, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": wl.WORKLOADS["tiny"],
+    "decode_small": wl.custom("decode", B=3, context=3000, n_shards=5),
+    "decode_gqa8": wl.custom("decode", B=2, Hq=64, Hkv=8, context=1500, n_shards=4),
+    "shortq_small": wl.custom("shortq", q_len=77, context=2500, block_len=256, n_shards=7),
+    "varlen_small": wl.custom("varlen", B=4, ctx_range=(100, 3000), q_range=(1, 300), block_len=128,
+                              n_shards=6),
+    "largest_small": wl.custom("largest", q_len=64, context=5000, block_len=512, n_shards=3),
+    "noncausal_multi_q": wl.custom("shortq", causal=False, q_len=9, context=1000, block_len=128,
+                                   n_shards=4),
+    "bf16_d64": wl.custom("shortq", d=64, q_len=20, context=900, block_len=128, n_shards=3),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available()
+    K.lib()
+
+
+@pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_cases_every_element(name, kernel):
+    w = SMALL[name]
+    inp, run, out, lse = run_cuda(w, kernel=kernel)
+    o_ref, l_ref = full_reference(inp)
+    eo, el = max_errors(out, lse, o_ref, l_ref)
+    assert_close(w, eo, el, f"{name}/{K.KERNEL_NAMES.get(run.kernel_used())}")
+
+
+@pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
+@pytest.mark.parametrize("name", ["decode_small", "shortq_small", "varlen_small", "tiny"])
+def test_partials_match_oracle_partials(name, kernel):
+    """Each work item's (O_i, L_i) equals the oracle's partial over the oracle's own shard."""
+    w = SMALL[name]
+    inp, run, _, _ = run_cuda(w, kernel=kernel)
+    costs = oracle.block_costs(inp.q_len, inp.kv_len, w.block_len, w.causal)
+    sob, _ = oracle.lpt_assign(costs, w.n_shards)
+    sets = oracle.shard_key_sets(sob, inp.kv_len, w.block_len, w.n_shards)
+    work = run.work_host
+    off_items, n_items = work[8], work[2]
+    o_part = run.o_part.cpu().double()
+    l_part = run.lse_part.cpu().double()
+    cu = np.concatenate([[0], np.cumsum(inp.q_len)])
+    args = (inp.q.cpu(), inp.k_pool.cpu(), inp.v_pool.cpu(), inp.block_table.cpu(), inp.q_len,
+            inp.kv_len, w.block_len, w.causal, w.scale)
+    cache = {}
+    for i in range(n_items):
+        shard, seq, _, _, prow = work[off_items + 8 * i: off_items + 8 * i + 5].tolist()
+        if shard not in cache:
+            cache[shard] = oracle.partial(*args, key_blocks=sets[shard])
+        o_ref, l_ref = cache[shard]
+        lq = inp.q_len[seq]
+        sl = slice(int(cu[seq]), int(cu[seq]) + lq)
+        eo, el = max_errors(o_part[prow: prow + lq], l_part[prow: prow + lq], o_ref[sl], l_ref[sl])
+        assert_close(w, eo, el, f"{name} item {i} (shard {shard}, seq {seq})")
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_full_size_workloads_sampled_rows(name):
+    """The five workloads at full size, auto kernel (what the benchmark runs), sampled rows."""
+    w = wl.WORKLOADS[name]
+    inp, run, out, lse = run_cuda(w, kernel=K.KERNEL_AUTO)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rows = sample_rows(inp, 48 if name != "tiny" else 64, seed=7)
+    eo, el = compare_rows(inp, out, lse, rows)
+    assert_close(w, eo, el, f"{name}/{K.KERNEL_NAMES.get(run.kernel_used())}")
+    assert K.splitkv_device_status() == 0
+
+
+def test_more_shards_than_blocks():
+    w = wl.custom("decode", B=1, context=700, n_shards=9)  # 3 blocks, 6 empty shards
+    inp, run, out, lse = run_cuda(w)
+    assert (run.shard_load == 0).sum() == 6
+    eo, el = max_errors(out, lse, *full_reference(inp))
+    assert_close(w, eo, el)
+
+
+def test_single_shard():
+    w = wl.custom("shortq", q_len=33, context=1200, block_len=256, n_shards=1)
+    inp, run, out, lse = run_cuda(w)
+    assert run.n_items == 1
+    eo, el = max_errors(out, lse, *full_reference(inp))
+    assert_close(w, eo, el)
+
+
+@pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
+def test_ragged_batch_with_empty_and_single_key_sequences(kernel):
+    w = wl.custom("varlen", B=4, block_len=128, n_shards=5)
+    lens = ([0, 1, 130, 7], [5, 1, 400, 7])  # no queries; one key; several tiles; one short block
+    inp, run, out, lse = run_cuda(w, kernel=kernel, lens=lens)
+    eo, el = max_errors(out, lse, *full_reference(inp))
+    assert_close(w, eo, el)
+
+
+def test_runs_are_deterministic():
+    w = SMALL["varlen_small"]
+    _, _, out1, lse1 = run_cuda(w)
+    _, _, out2, lse2 = run_cuda(w)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_out_of_range_block_is_reported_not_read():
+    w = wl.custom("decode", B=2, context=1000, n_shards=3)
+    inp = wl.make_inputs(w, device="cuda")
+    K.splitkv_device_status(clear=True)
+    bad = inp.block_table.clone()
+    bad[1, 2] = inp.n_pool_blocks + 5
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype)
+    run(inp.q, inp.k_pool, inp.v_pool, bad, w.scale)
+    torch.cuda.synchronize()
+    assert K.splitkv_device_status(clear=True) & 1
+    assert K.splitkv_device_status() == 0
+    out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    torch.cuda.synchronize()
+    eo, el = max_errors(out, lse, *full_reference(inp))
+    assert_close(w, eo, el)
+
+
+def test_bad_arguments_raise_before_launch():
+    w = SMALL["decode_small"]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype)
+    with pytest.raises(K.SplitKVError):
+        K.splitkv_attn_partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, run.work_device,
+                               run.n_items, run.B, run.total_q, run.max_q_len, w.block_len, float("nan"),
+                               w.causal, run._o_part, run._lse_part)
+    with pytest.raises(K.SplitKVError):  # tensor-core kernel does not take block_len % 128 != 0
+        w2 = wl.custom("shortq", q_len=40, context=1000, block_len=200, n_shards=2)
+        run_cuda(w2, kernel=K.KERNEL_TC)

@@ -1,0 +1,184 @@
+"""Host-side checks of the C ABI (no GPU): exports, block costs, LPT plan, work lists, errors.
+
+The C++ planner must reproduce the oracle's LPT plan bit for bit (integer
+costs, fixed tie order), on every workload and on random fuzz cases.
+"""
+
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from context_long_attention_lpt_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def k():
+    from context_long_attention_lpt_gb300 import build, splitkv
+
+    if not os.path.exists(splitkv.library_path()):
+        build.build()
+    splitkv.lib()
+    return splitkv
+
+
+def _header_symbols():
+    text = open(os.path.join(ROOT, "include", "splitkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(splitkv_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(k):
+    syms = _header_symbols()
+    assert len(syms) >= 10
+    L = k.lib()
+    for s in syms:
+        assert hasattr(L, s), s
+    assert set(syms) == set(k.exported_symbols())
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_costs_and_plan_match_oracle_on_workloads(k, name):
+    w = wl.WORKLOADS[name]
+    q, kv = wl.lengths(w)
+    costs = k.splitkv_block_costs(q, kv, w.block_len, w.causal)
+    ref_costs = oracle.block_costs(q, kv, w.block_len, w.causal)
+    assert costs.tolist() == ref_costs
+    sob, load = k.splitkv_plan(costs, w.n_shards)
+    ref_sob, ref_load = oracle.lpt_assign(ref_costs, w.n_shards)
+    assert sob.tolist() == ref_sob
+    assert load.tolist() == ref_load
+
+
+def test_fuzz_costs_and_plans_bit_exact(k):
+    rng = random.Random(1234)
+    for case in range(3000):
+        B = rng.randint(1, 4)
+        causal = rng.random() < 0.6
+        q = [rng.randint(0, 40) for _ in range(B)]
+        kv = [qq + rng.randint(0 if qq else 1, 200) for qq in q]
+        bl = rng.choice([1, 3, 8, 16, 64])
+        S = rng.randint(1, 9)
+        costs = k.splitkv_block_costs(q, kv, bl, causal)
+        ref = oracle.block_costs(q, kv, bl, causal)
+        assert costs.tolist() == ref, (case, q, kv, bl, causal)
+        sob, load = k.splitkv_plan(costs, S)
+        rsob, rload = oracle.lpt_assign(ref, S)
+        assert sob.tolist() == rsob and load.tolist() == rload, case
+
+
+def test_fuzz_plans_with_many_ties(k):
+    rng = random.Random(99)
+    for case in range(2000):
+        n = rng.randint(0, 60)
+        costs = [rng.choice([0, 1, 2, 5, 5, 5, 9]) for _ in range(n)]
+        S = rng.randint(1, 12)
+        sob, load = k.splitkv_plan(np.array(costs, dtype=np.int64), S)
+        rsob, rload = oracle.lpt_assign(costs, S)
+        assert sob.tolist() == rsob and load.tolist() == rload, case
+
+
+def _decode_work(work):
+    hdr = work[:16]
+    assert hdr[0] == 0x534B5631
+    B, n_items, n_shards, bl, total_q, max_q = hdr[1:7]
+    off_seq, off_items, off_blocks, off_seq_items, n_blocks = hdr[7:12]
+    seqs = work[off_seq: off_seq + 4 * (B + 1)].reshape(B + 1, 4)
+    items = work[off_items: off_items + 8 * n_items].reshape(n_items, 8)
+    blocks = work[off_blocks: off_blocks + n_blocks]
+    seq_items = work[off_seq_items: off_seq_items + n_items]
+    return dict(B=B, n_items=n_items, total_q=total_q, max_q=max_q, seqs=seqs, items=items,
+                blocks=blocks, seq_items=seq_items, n_blocks=n_blocks)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_work_lists_cover_the_plan(k, name):
+    w = wl.WORKLOADS[name]
+    q, kv = wl.lengths(w)
+    costs = k.splitkv_block_costs(q, kv, w.block_len, w.causal)
+    sob, _ = k.splitkv_plan(costs, w.n_shards)
+    work, n_items, part_rows = k.splitkv_build_work(q, kv, w.block_len, costs, sob, w.n_shards)
+    d = _decode_work(work)
+    assert d["n_items"] == n_items and d["total_q"] == sum(q) and d["max_q"] == max(q)
+    sets = oracle.shard_key_sets(sob.tolist(), kv, w.block_len, w.n_shards)
+    seen = set()
+    rows = 0
+    item_costs = []
+    gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
+    for i, it in enumerate(d["items"]):
+        shard, seq, off, cnt, prow, clo, chi, _ = it.tolist()
+        blks = d["blocks"][off: off + cnt].tolist()
+        assert blks == sets[shard][seq] and cnt > 0
+        for j in blks:
+            assert (seq, j) not in seen
+            seen.add((seq, j))
+        assert prow == rows
+        rows += q[seq]
+        cost = (clo & 0xFFFFFFFF) | (chi << 32)
+        assert cost == sum(costs[gbase[seq] + j] for j in blks)
+        item_costs.append(cost)
+    assert len(seen) == len(costs)
+    assert rows == part_rows
+    assert item_costs == sorted(item_costs, reverse=True)
+    # per-sequence item lists: every item of the sequence, ascending shard
+    for b in range(len(q)):
+        p0, p1 = d["seqs"][b, 3], d["seqs"][b + 1, 3]
+        its = d["seq_items"][p0:p1].tolist()
+        assert all(d["items"][i, 1] == b for i in its)
+        assert [d["items"][i, 0] for i in its] == sorted(d["items"][i, 0] for i in its)
+        assert sorted(its) == sorted(i for i in range(n_items) if d["items"][i, 1] == b)
+        assert d["seqs"][b, 0] == sum(q[:b]) and d["seqs"][b, 1] == q[b] and d["seqs"][b, 2] == kv[b]
+
+
+def test_imbalance_on_workloads(k):
+    """Report max/mean - 1 of the LPT loads; the hand-derived values are pinned in test_oracle."""
+    for name in wl.WORKLOADS:
+        w = wl.WORKLOADS[name]
+        q, kv = wl.lengths(w)
+        _, load = k.splitkv_plan(k.splitkv_block_costs(q, kv, w.block_len, w.causal), w.n_shards)
+        assert abs((load.max() / load.mean() - 1) - oracle.imbalance(load.tolist())) < 1e-12
+
+
+def test_errors_are_statuses_not_crashes(k):
+    L = k.lib()
+    assert L.splitkv_plan(None, 5, 2, None, None) < 0
+    assert "bad block arrays" in k.splitkv_last_error()
+    c = np.array([1, 2, 3], dtype=np.int64)
+    sob = np.zeros(3, dtype=np.int32)
+    load = np.zeros(1, dtype=np.int64)
+    assert L.splitkv_plan(c.ctypes.data_as(ctypes.c_void_p), 3, 0, sob.ctypes.data_as(ctypes.c_void_p),
+                          load.ctypes.data_as(ctypes.c_void_p)) < 0
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_block_costs([5], [3], 4, True)  # q_len > kv_len
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_build_work([1], [4], 2, [1, 1], [0, 7], 2)  # shard id out of range
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_num_blocks([4], 0)
+    # device entry points validate before touching the GPU
+    assert L.splitkv_attn_partial(None, None, None, 0, None, 0, None, 1, 1, 1, 1, 4, 3, 128, 128,
+                                  1.0, 0, 1, None, None, 0, 0, None) == -1
+    assert L.splitkv_attn_partial(None, None, None, 0, None, 0, None, 1, 1, 1, 1, 4, 4, 96, 128,
+                                  1.0, 0, 1, None, None, 0, 0, None) == -2
+    assert L.splitkv_merge(None, None, 0, None, 1, 4, 4, 128, 5, None, None, None) == -1
+    assert L.splitkv_auto_kernel(4, 3, 128, 128, 1, 1) < 0
+
+
+def test_work_buffer_too_small_is_capacity_error(k):
+    L = k.lib()
+    q = np.array([2], dtype=np.int32)
+    kv = np.array([9], dtype=np.int32)
+    c = k.splitkv_block_costs(q, kv, 4, True)
+    sob, _ = k.splitkv_plan(c, 2)
+    work = np.zeros(4, dtype=np.int32)
+    n_items = ctypes.c_int32()
+    rows = ctypes.c_int64()
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = L.splitkv_build_work(p(q), p(kv), 1, 4, p(c), p(sob), len(c), 2, p(work), 4,
+                              ctypes.byref(n_items), ctypes.byref(rows))
+    assert st == -4
