@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--context", type=int, default=None,
+                    help="override the context length (smaller cases for profiling)")
     return ap.parse_args(argv)
 
 
@@ -209,6 +211,8 @@ def run_ours(args, dctx):
     torch.cuda.set_device(dev)
     K.lib()
     w = wl.WORKLOADS[args.workload]
+    if args.context:
+        w = wl.custom(w, context=args.context)
     kernel = {"auto": K.KERNEL_AUTO, "simt": K.KERNEL_SIMT, "decode": K.KERNEL_DECODE,
               "tc": K.KERNEL_TC}[args.kernel]
     inp = wl.make_inputs(w, device=f"cuda:{dev}")
