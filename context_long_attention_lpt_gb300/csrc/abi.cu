@@ -87,24 +87,26 @@ extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const voi
   }
   const int k = pick_kernel(a, kernel);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  int st = SPLITKV_OK;
   switch (k) {
     case SPLITKV_KERNEL_TC:
       if (!splitkv::tc_supports(a))
         return fail(SPLITKV_ERR_UNSUPPORTED, "tensor-core kernel needs bf16, d=128, block_len %% 128 == 0, "
-                    "128 %% G == 0");
-      e = splitkv::launch_partial_tc(a, s);
+                    "G dividing 128");
+      st = splitkv::launch_partial_tc(a, s);
       break;
     case SPLITKV_KERNEL_DECODE:
       if (!splitkv::decode_supports(a))
-        return fail(SPLITKV_ERR_UNSUPPORTED, "decode kernel needs bf16, d=128 and q_len*G <= 16");
-      e = splitkv::launch_partial_decode(a, s);
+        return fail(SPLITKV_ERR_UNSUPPORTED, "decode kernel needs bf16, d=128, q_len*G <= 8, block_len %% 64 == 0");
+      st = splitkv::launch_partial_decode(a, s);
       break;
-    default:
-      e = splitkv::launch_partial_simt(a, s);
+    default: {
+      const cudaError_t e = splitkv::launch_partial_simt(a, s);
+      if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "partial launch: %s", cudaGetErrorString(e));
       break;
+    }
   }
-  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "partial launch: %s", cudaGetErrorString(e));
+  if (st != SPLITKV_OK) return st;
   splitkv::clear_error();
   return SPLITKV_OK;
 }

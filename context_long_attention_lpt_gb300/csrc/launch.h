@@ -37,8 +37,9 @@ struct PartialArgs {
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);
-cudaError_t launch_partial_decode(const PartialArgs& a, cudaStream_t stream);
-cudaError_t launch_partial_tc(const PartialArgs& a, cudaStream_t stream);
+// The specialised kernels return a SPLITKV_* status (they also encode TMA maps).
+int launch_partial_decode(const PartialArgs& a, cudaStream_t stream);
+int launch_partial_tc(const PartialArgs& a, cudaStream_t stream);
 
 // Shape limits of the specialised kernels (checked before launching them).
 bool decode_supports(const PartialArgs& a);

@@ -1,72 +1,96 @@
 // CUDA-core partial attention for decode-shaped work: bf16, d = 128,
-// q_len * G <= 8 query rows per (sequence, K/V head).
+// q_len * G <= 8 query rows per (sequence, K/V head), block_len % 64 == 0.
 //
 // The Split-KV card's local step ("Timeline": each shard attends over its own
-// KV blocks) is, for one query token, a read of every K/V row of the shard's
-// blocks once: the kernel is bound by HBM bandwidth, so the design goal is
-// coalesced 128-bit loads with many bytes in flight and few instructions per
-// byte.
+// KV blocks) is, for a single query token, one read of every K/V row of the
+// shard's blocks: the kernel is bound by HBM bandwidth.  The design keeps many
+// bytes in flight with few instructions per byte:
 //
-// One CTA (4 warps) takes one (work item, K/V head) unit.  A half-warp owns one
-// 256-byte K (or V) row per load: lane i of the half-warp loads d-elements
-// [8i, 8i+8) with one 16-byte load, so each row is two full 128-byte lines.
-// A warp processes batches of 2*KPB keys (KPB per half-warp); the next batch
-// is prefetched into registers while the current one is computed.
+// * One CTA takes one (work item, K/V head) unit.  A producer warp streams the
+//   unit's K and V rows with TMA (3-D tiled bulk copies of 64 keys x 256 B out
+//   of the paged pool viewed as [tokens, Hkv, d]) into a ring of kStages
+//   shared-memory stages, each guarded by a full and an empty mbarrier.
+// * Four consumer warps read the stages.  A half-warp works on one key row at
+//   a time: lane i holds d-elements [8i, 8i+8) (one 16-byte shared load), and
+//   per batch a half-warp takes KPB keys, so a lane computes KPB keys x R rows
+//   = 16 partial dot products with packed fp32x2 FMAs.
+// * A four-step butterfly over the half-warp (xor 8, 4, 2, 1) sums them.  Each
+//   lane reads its keys and query rows in an order permuted by its own lane
+//   index (slot i holds logical value i XOR lane), so every step is one shuffle
+//   and one add with no selects; afterwards lane i holds the full score of
+//   logical value i = key * R + row.
+// * Online softmax in base 2 (queries pre-scaled by scale*log2 e): per row a
+//   running max m and sum l over lanes sharing the row; P.V accumulates in
+//   per-lane fp32x2 registers acc[row][8].  At the end the two half-warps and
+//   the four warps are combined exactly through shared memory and the unit's
+//   partial (O_i, L_i) is written.
 //
-// Scores: every lane has partial dot products over its 8 elements for KPB keys
-// x R rows = 16 values.  A four-step butterfly (xor 8, 4, 2, 1) halves the
-// values per lane at each step while summing across the half-warp, leaving lane
-// i with the full score of value i = key * R + row: 15 shuffles for 16 scores.
-// The online softmax (running max m, running sum l, in base 2 with the query
-// pre-scaled by scale*log2(e)) then runs per row over lanes sharing the row,
-// and P.V accumulates into per-lane registers acc[row][8].  At the end the two
-// half-warps and the 4 warps are combined exactly (max / rescaled sums)
-// through shared memory and the unit's partial (O_i, L_i) is written.
+// Keys past the sequence end or a row's causal limit get score -inf and their
+// V rows are replaced by zeros, so whatever the pool holds there (NaN
+// included) never reaches the result.
 
 #include <cmath>
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
+#include "status.h"
+#include "tensor_map.h"
 
 namespace splitkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kWarps = 4;
+constexpr int kKT = 64;                       // keys per TMA tile
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr uint32_t kTileBytes = kKT * kD * 2;  // one K (or V) tile
+constexpr size_t kSmemBytes = kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) + 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
+// Tiles of a work item: for each of its blocks the keys [lo, lo + n) that some
+// row of the unit can see, cut into kKT-key tiles.  Producer and consumers
+// walk the same sequence.
+struct TileWalk {
+  const int32_t* blocks;
+  const int32_t* table;
+  int32_t blk_cnt, bl, max_blocks, kv_len, vis_max;
+  int64_t n_pool;
 
-// One butterfly step over N values: lanes whose `mask` bit is set keep the
-// upper half, the others the lower half; each kept value adds the partner's.
-template <int N>
-__device__ __forceinline__ void butterfly(float (&v)[16], bool upper, int mask) {
-#pragma unroll
-  for (int j = 0; j < N / 2; ++j) {
-    const float send = upper ? v[j] : v[j + N / 2];
-    const float keep = upper ? v[j + N / 2] : v[j];
-    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+  // Returns the physical block of block bi and its visible key count (0: skip it).
+  __device__ __forceinline__ int32_t block(int32_t bi, int32_t* lo, int32_t* n, bool* bad) const {
+    const int32_t j = __ldg(blocks + bi);
+    *lo = j * bl;
+    *n = min(min(bl, kv_len - *lo), vis_max - *lo);
+    *bad = false;
+    if (*n <= 0) return -1;
+    const int32_t phys = j < max_blocks ? __ldg(table + j) : -1;
+    if (phys < 0 || phys >= n_pool) {
+      *bad = true;
+      return -1;
+    }
+    return phys;
   }
-}
+};
 
 template <int R>
-__global__ void __launch_bounds__(kWarps * 32, R == 4 ? 3 : 2) partial_decode_kernel(PartialArgs a) {
-  constexpr int KPB = 16 / R;   // keys per half-warp per batch
-  constexpr int KPW = 2 * KPB;  // keys per warp per batch
-  __shared__ float sm_acc[kWarps][R][kD];
-  __shared__ float sm_m[kWarps][R];
-  __shared__ float sm_l[kWarps][R];
+__global__ void __launch_bounds__(kThreads, 2)
+    partial_decode_kernel(PartialArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v) {
+  constexpr int KPB = 16 / R;               // keys per half-warp per batch
+  constexpr int KPW = 2 * KPB;              // keys per warp per batch
+  constexpr int BPW = kKT / (kConsumerWarps * KPW);  // batches per warp per tile
+  static_assert(BPW * kConsumerWarps * KPW == kKT, "tile split");
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stage_k = smem;
+  uint8_t* stage_v = smem + kStages * kTileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kTileBytes);
+  uint64_t* empty = full + kStages;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int hw = lane >> 4, li = lane & 15;
   const int32_t item = blockIdx.x / a.Hkv;
   const int32_t kvh = blockIdx.x % a.Hkv;
 
@@ -84,172 +108,212 @@ __global__ void __launch_bounds__(kWarps * 32, R == 4 ? 3 : 2) partial_decode_ke
     if (threadIdx.x == 0) atomicOr(a.status, 2u);
     return;
   }
+  const TileWalk walk{wv.blocks() + blk_off,
+                      a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq,
+                      blk_cnt, a.block_len, a.max_blocks_per_seq, kv_len,
+                      visible_keys(q_len, kv_len, (rows - 1) / G, a.causal), a.n_pool_blocks};
 
-  // Query rows (token r / G, head kvh*G + r % G), this lane's 8 elements, scaled to base 2.
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const float qscale = a.scale * kLog2e;
-  float qf[R][8];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (r < rows) {
-      const int64_t qi = (static_cast<int64_t>(cu_q + r / G) * a.Hq + kvh * G + r % G) * kD + 8 * li;
-      float f[8];
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q + qi)), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[r][e] = f[e] * qscale;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[r][e] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], kConsumerWarps);
     }
-  }
-  // This lane's score after the butterfly belongs to row li % R.
-  const int my_row = li % R;
-  const int32_t my_vis = my_row < rows ? visible_keys(q_len, kv_len, my_row / G, a.causal) : 0;
-
-  const uint4* kp = static_cast<const uint4*>(a.k_pool);
-  const uint4* vp = static_cast<const uint4*>(a.v_pool);
-  const int32_t bl = a.block_len;
-  const int32_t* blocks = wv.blocks() + blk_off;
-  const int32_t* table = a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
-  const int64_t n_batches = static_cast<int64_t>(blk_cnt) * (bl / KPW);
-  const int64_t row_stride = static_cast<int64_t>(a.Hkv) * (kD / 8);  // uint4 per token
-
-  // Loads the K/V rows of batch `b` for this half-warp; returns the position of
-  // its first key (or -1 if the batch's block is unusable).  Keys past the
-  // sequence end are not read (zeros), so their slots never carry NaN.
-  auto load = [&](int64_t b, uint4 (&kb)[KPB], uint4 (&vb)[KPB]) -> int32_t {
-    const int32_t bi = static_cast<int32_t>(b / (bl / KPW));
-    const int32_t off = static_cast<int32_t>(b % (bl / KPW)) * KPW + hw * KPB;
-    const int32_t j = __ldg(blocks + bi);
-    int32_t phys = j < a.max_blocks_per_seq ? __ldg(table + j) : -1;
-    if (phys < 0 || phys >= a.n_pool_blocks) {
-      if (lane == 0) atomicOr(a.status, 1u);
-      phys = -1;
-    }
-    const int32_t pos0 = j * bl + off;
-    const int64_t base = ((static_cast<int64_t>(phys) * bl + off) * a.Hkv + kvh) * (kD / 8) + li;
-#pragma unroll
-    for (int k = 0; k < KPB; ++k) {
-      if (phys >= 0 && pos0 + k < kv_len) {
-        kb[k] = __ldg(kp + base + k * row_stride);
-        vb[k] = __ldg(vp + base + k * row_stride);
-      } else {
-        kb[k] = make_uint4(0, 0, 0, 0);
-        vb[k] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    return phys >= 0 ? pos0 : -1;
-  };
-
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[R][8];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
-
-  uint4 kc[KPB], vc[KPB], kn[KPB], vn[KPB];
-  int64_t b = warp;
-  int32_t pos_c = b < n_batches ? load(b, kc, vc) : -1;
-  for (; b < n_batches; b += kWarps) {
-    const int64_t bn = b + kWarps;
-    int32_t pos_n = -1;
-    if (bn < n_batches) pos_n = load(bn, kn, vn);
-
-    // partial dot products: v[k*R + r] over this lane's 8 elements
-    float v[16];
-#pragma unroll
-    for (int k = 0; k < KPB; ++k) {
-      float kf[8];
-      bf16x8_to_f32(kc[k], kf);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(qf[r][e], kf[e], s);
-        v[k * R + r] = s;
-      }
-    }
-    butterfly<16>(v, li & 8, 8);
-    butterfly<8>(v, li & 4, 4);
-    butterfly<4>(v, li & 2, 2);
-    butterfly<2>(v, li & 1, 1);
-    // lane holds the score of key (hw*KPB + li / R) for row li % R
-    const int32_t pos = pos_c + li / R;
-    float s = v[0];
-    if (pos_c < 0 || pos >= kv_len || pos >= my_vis) s = -INFINITY;
-    float bmax = s;
-#pragma unroll
-    for (int m = R; m < 32; m <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, m));
-    const float m_new = fmaxf(m_run, bmax);
-    float p = 0.f, alpha = 1.f;
-    if (m_new != -INFINITY) {
-      p = exp2f(s - m_new);
-      alpha = exp2f(m_run - m_new);
-    }
-    float psum = p;
-#pragma unroll
-    for (int m = R; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float ar = __shfl_sync(0xffffffffu, alpha, (lane & 16) | r);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[r][e] *= ar;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < KPB; ++k) {
-      float vf[8];
-      bf16x8_to_f32(vc[k], vf);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float pk = __shfl_sync(0xffffffffu, p, (lane & 16) | (k * R + r));
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[r][e] = fmaf(pk, vf[e], acc[r][e]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < KPB; ++k) {
-      kc[k] = kn[k];
-      vc[k] = vn[k];
-    }
-    pos_c = pos_n;
-  }
-
-  // The two half-warps saw different keys under the same running max: add them.
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], 16);
-  if (hw == 0) {
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm_acc[warp][r][8 * li + e] = acc[r][e];
-    if (li < R) {
-      sm_m[warp][li] = m_run;
-      sm_l[warp][li] = l_run;
-    }
+    ptx::fence_mbar_init();
   }
   __syncthreads();
 
-  // Exact combination of the warps' running (m, l, acc), then the unit's partial.
-  for (int i = threadIdx.x; i < R * kD; i += kWarps * 32) {
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+      int32_t t = 0;
+      bool ok = true;
+      for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
+        int32_t lo, n;
+        bool bad;
+        const int32_t phys = walk.block(bi, &lo, &n, &bad);
+        if (bad) atomicOr(a.status, 1u);
+        if (phys < 0) continue;
+        for (int32_t off = 0; off < n; off += kKT, ++t) {
+          const int s = t % kStages;
+          if (t >= kStages && !ptx::mbar_wait(&empty[s], ((t / kStages) & 1) ^ 1)) {
+            atomicOr(a.status, ptx::kStatusTimeout);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+          const int32_t row = phys * a.block_len + off;
+          ptx::tma_load_3d(stage_k + s * kTileBytes, &tmap_k, 0, kvh, row, &full[s]);
+          ptx::tma_load_3d(stage_v + s * kTileBytes, &tmap_v, 0, kvh, row, &full[s]);
+        }
+      }
+      // Copies still in flight land before this CTA's shared memory goes away.
+      for (int32_t u = max(0, t - kStages); u < t; ++u)
+        if (!ptx::mbar_wait(&full[u % kStages], (u / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int hw = lane >> 4, li = lane & 15;
+  const int rot_k = li / R, rot_r = li % R;  // this lane's slot permutation
+  float2 qf[R][4];
+  float m_run = -INFINITY, l_run = 0.f;
+  float2 acc[R][4];
+  int32_t my_vis = 0;
+  if (warp < kConsumerWarps) {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    const float qscale = a.scale * kLog2e;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int row = r ^ rot_r;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (row < rows) {
+        const int64_t qi = (static_cast<int64_t>(cu_q + row / G) * a.Hq + kvh * G + row % G) * kD + 8 * li;
+        u = __ldg(reinterpret_cast<const uint4*>(q + qi));
+      }
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = ptx::bf16x2_to_f32x2(w4[e]);
+        qf[r][e] = make_float2(f.x * qscale, f.y * qscale);
+        acc[r][e] = make_float2(0.f, 0.f);
+      }
+    }
+    my_vis = rot_r < rows ? visible_keys(q_len, kv_len, rot_r / G, a.causal) : 0;
+
+    int32_t t = 0;
+    bool ok = true;
+    for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
+      int32_t lo, n;
+      bool bad;
+      const int32_t phys = walk.block(bi, &lo, &n, &bad);
+      if (phys < 0) continue;
+      for (int32_t off = 0; off < n; off += kKT, ++t) {
+        const int s = t % kStages;
+        if (!ptx::mbar_wait(&full[s], (t / kStages) & 1)) {
+          if (lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+          ok = false;
+          break;
+        }
+        const int32_t nvalid = min(kKT, n - off);
+        const int32_t pos0 = lo + off;
+        const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(stage_k + s * kTileBytes);
+        const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(stage_v + s * kTileBytes);
+#pragma unroll
+        for (int bb = 0; bb < BPW; ++bb) {
+          const int32_t half_base = (warp * BPW + bb) * KPW + hw * KPB;
+          // partial dot products in permuted slots
+          float v[16];
+#pragma unroll
+          for (int k = 0; k < KPB; ++k) {
+            const int key = half_base + (k ^ rot_k);
+            const uint4 u = *reinterpret_cast<const uint4*>(ks + key * kD + 8 * li);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            float2 kf[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kf[e] = ptx::bf16x2_to_f32x2(w4[e]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d2 = ptx::ffma2(qf[r][e], kf[e], d2);
+              v[k * R + r] = d2.x + d2.y;
+            }
+          }
+#pragma unroll
+          for (int m = 8, nv = 16; m >= 1; m >>= 1, nv >>= 1)
+#pragma unroll
+            for (int j = 0; j < nv / 2; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j + nv / 2], m);
+          // lane holds the score of key half_base + li / R for row li % R
+          const int32_t key = half_base + li / R;
+          float sc = v[0];
+          if (key >= nvalid || pos0 + key >= my_vis) sc = -INFINITY;
+          float bmax = sc;
+#pragma unroll
+          for (int m = R; m < 32; m <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, m));
+          const float m_new = fmaxf(m_run, bmax);
+          float p = 0.f, alpha = 1.f;
+          if (m_new != -INFINITY) {
+            p = exp2f(sc - m_new);
+            alpha = exp2f(m_run - m_new);
+          }
+          float psum = p;
+#pragma unroll
+          for (int m = R; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
+          l_run = l_run * alpha + psum;
+          m_run = m_new;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float ar = __shfl_sync(0xffffffffu, alpha, (lane & 16) | r);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[r][e] = make_float2(acc[r][e].x * ar, acc[r][e].y * ar);
+            }
+          }
+          const bool tail = nvalid < kKT;
+#pragma unroll
+          for (int k = 0; k < KPB; ++k) {
+            const int key_k = half_base + k;
+            uint4 u = *reinterpret_cast<const uint4*>(vs + key_k * kD + 8 * li);
+            if (tail && key_k >= nvalid) u = make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            float2 vf[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vf[e] = ptx::bf16x2_to_f32x2(w4[e]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float pk = __shfl_sync(0xffffffffu, p, (lane & 16) | (k * R + r));
+              const float2 pp = make_float2(pk, pk);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[r][e] = ptx::ffma2(pp, vf[e], acc[r][e]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[s]);
+      }
+    }
+    // The two half-warps saw different keys under the same running max.
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[r][e].x += __shfl_xor_sync(0xffffffffu, acc[r][e].x, 16);
+        acc[r][e].y += __shfl_xor_sync(0xffffffffu, acc[r][e].y, 16);
+      }
+  }
+  __syncthreads();  // pipeline drained: the stage memory is free for the combine
+
+  float* sm_acc = reinterpret_cast<float*>(smem);            // [warps][R][kD]
+  float* sm_m = sm_acc + kConsumerWarps * R * kD;            // [warps][R]
+  float* sm_l = sm_m + kConsumerWarps * R;
+  if (warp < kConsumerWarps && hw == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        reinterpret_cast<float2*>(sm_acc + (warp * R + r) * kD + 8 * li)[e] = acc[r][e];
+    if (li < R) {
+      sm_m[warp * R + li] = m_run;
+      sm_l[warp * R + li] = l_run;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * kD; i += kThreads) {
     const int r = i / kD, c = i % kD;
     if (r >= rows) continue;
     float mx = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, sm_m[w][r]);
+    for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, sm_m[w * R + r]);
     float l = 0.f, o = 0.f;
     if (mx != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(sm_m[w][r] - mx);
-        l += sm_l[w][r] * f;
-        o += sm_acc[w][r][c] * f;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = exp2f(sm_m[w * R + r] - mx);
+        l += sm_l[w * R + r] * f;
+        o += sm_acc[(w * R + r) * kD + c] * f;
       }
     }
     const int64_t orow = static_cast<int64_t>(part_row + r / G) * a.Hq + kvh * G + r % G;
@@ -258,24 +322,44 @@ __global__ void __launch_bounds__(kWarps * 32, R == 4 ? 3 : 2) partial_decode_ke
   }
 }
 
+template <int R>
+int launch_r(const PartialArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  auto kern = partial_decode_kernel<R>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "decode smem attribute: %s", cudaGetErrorString(e));
+  const int64_t grid = static_cast<int64_t>(a.n_items) * a.Hkv;
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return SPLITKV_OK;
+}
+
 }  // namespace
 
 bool decode_supports(const PartialArgs& a) {
   if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
   const int64_t rows = static_cast<int64_t>(a.max_q_len) * (a.Hq / a.Hkv);
-  return rows >= 1 && rows <= 8 && a.block_len % 8 == 0;
+  return rows >= 1 && rows <= 8 && a.block_len % kKT == 0 &&
+         static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
 }
 
-cudaError_t launch_partial_decode(const PartialArgs& a, cudaStream_t stream) {
+int launch_partial_decode(const PartialArgs& a, cudaStream_t stream) {
   const int64_t grid = static_cast<int64_t>(a.n_items) * a.Hkv;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (grid == 0) return SPLITKV_OK;
+  if (grid > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many work units");
+  // K/V pools as [tokens, Hkv, d] bf16; one box = 64 tokens of one head.
+  const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hkv),
+                            static_cast<uint64_t>(a.n_pool_blocks) * a.block_len};
+  const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hkv) * kD * 2ull};
+  const uint32_t box[3] = {kD, 1, kKT};
+  CUtensorMap tk, tv;
+  int st = encode_bf16_3d(&tk, a.k_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != SPLITKV_OK) return st;
+  st = encode_bf16_3d(&tv, a.v_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != SPLITKV_OK) return st;
   const int64_t rows = static_cast<int64_t>(a.max_q_len) * (a.Hq / a.Hkv);
-  if (rows <= 4)
-    partial_decode_kernel<4><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(a);
-  else
-    partial_decode_kernel<8><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  return rows <= 4 ? launch_r<4>(a, tk, tv, stream) : launch_r<8>(a, tk, tv, stream);
 }
 
 }  // namespace splitkv

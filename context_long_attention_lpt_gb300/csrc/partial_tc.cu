@@ -2,5 +2,5 @@
 
 namespace splitkv {
 bool tc_supports(const PartialArgs&) { return false; }
-cudaError_t launch_partial_tc(const PartialArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+int launch_partial_tc(const PartialArgs&, cudaStream_t) { return SPLITKV_ERR_UNSUPPORTED; }
 }  // namespace splitkv

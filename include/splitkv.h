@@ -54,7 +54,7 @@ extern "C" {
 /* kernel choice for splitkv_attn_partial */
 #define SPLITKV_KERNEL_AUTO 0   /* pick the fastest kernel that supports the shape */
 #define SPLITKV_KERNEL_SIMT 1   /* generic CUDA-core kernel: any shape, fp32 or bf16 */
-#define SPLITKV_KERNEL_DECODE 2 /* CUDA-core decode kernel: bf16, d=128, q_len*G <= 16 */
+#define SPLITKV_KERNEL_DECODE 2 /* CUDA-core decode kernel: bf16, d=128, q_len*G <= 8, block_len%64==0 */
 #define SPLITKV_KERNEL_TC 3     /* TMA + tcgen05/TMEM kernel: bf16, d=128, block_len%128==0 */
 
 /* ---------------------------------------------------------------- host side */
