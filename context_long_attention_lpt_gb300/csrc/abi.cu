@@ -28,10 +28,12 @@ unsigned int* status_word(int* err) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Decode kernel for a handful of query rows per K/V head, tensor cores once the
+// rows fill MMA tiles, the generic CUDA-core kernel for everything else.
 int pick_kernel(const splitkv::PartialArgs& a, int32_t requested) {
   if (requested != SPLITKV_KERNEL_AUTO) return requested;
-  if (splitkv::tc_supports(a)) return SPLITKV_KERNEL_TC;
   if (splitkv::decode_supports(a)) return SPLITKV_KERNEL_DECODE;
+  if (splitkv::tc_supports(a)) return SPLITKV_KERNEL_TC;
   return SPLITKV_KERNEL_SIMT;
 }
 

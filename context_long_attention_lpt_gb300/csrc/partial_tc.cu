@@ -1,6 +1,469 @@
+// Tensor-core partial attention for sm_103a: TMA + tcgen05 (UMMA) + TMEM.
+//
+// Used when the query rows of a (sequence, K/V head) pair fill tensor-core
+// tiles: bf16, d = 128, block_len % 128 == 0, G = Hq / Hkv dividing 128.
+// Computes, for every work item (a shard's blocks of one sequence), the
+// shard's partial (O_i, L_i) of the Split-KV card's local attention step
+// ("Timeline": keys and values stay local; only a query-sized result leaves).
+//
+// One CTA = one (work item, K/V head, tile of 128 query rows); row r of the
+// tile is token r / G, query head kvh*G + r % G, so the G heads sharing a K/V
+// head share every K/V tile.  Warp roles (192 threads):
+//   warps 0-3  softmax + epilogue: thread i owns row i (TMEM lane i);
+//   warp 4     TMA producer: Q once, then K and V tiles of 128 keys from the
+//              paged pool (3-D maps over [tokens, Hkv, d], 128-byte swizzle,
+//              two 64-column halves per tile) into kStagesK / kStagesV rings;
+//   warp 5     TMEM allocation and MMA issue (one elected lane).
+// Per KV tile j:  S_j = Q K_j^T     tcgen05.mma kind::f16, M=N=128, fp32 in
+//                                   TMEM (two S buffers, alternating);
+//                 softmax_j         rows read S_j with tcgen05.ld, keep a
+//                                   running max/sum in base 2, write
+//                                   P_j = exp2(s*c - m) as bf16 into the first
+//                                   64 columns of S_j's buffer (tcgen05.st);
+//                 O += P_j V_j      tcgen05.mma with A = P_j from TMEM and
+//                                   B = V_j (MN-major) from shared memory.
+// The MMA warp issues S_{j+1} before waiting for P_j, so the tensor cores
+// compute the next scores while the softmax warps work.  The running max is
+// only moved (and O rescaled through TMEM) when it grows by more than 2^8, so
+// P stays <= 256 and the common tile needs no O traffic.
+//
+// Keys past the sequence end (pool slots that may hold anything) get score
+// -inf, and their V rows inside the last 16-key MMA step are zeroed in shared
+// memory before the P.V MMA, so they contribute exactly nothing.
+
+#include <cmath>
+
+#include "device_common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
+#include "status.h"
+#include "tc_ptx.cuh"
+#include "tensor_map.h"
 
 namespace splitkv {
-bool tc_supports(const PartialArgs&) { return false; }
-int launch_partial_tc(const PartialArgs&, cudaStream_t) { return SPLITKV_ERR_UNSUPPORTED; }
+namespace {
+
+constexpr int kD = 128;
+constexpr int kM = 128;   // query rows per CTA
+constexpr int kN = 128;   // keys per tile
+constexpr int kStagesK = 2;
+constexpr int kStagesV = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kHalfBytes = kN * 64 * 2;   // 128 rows x 64 bf16 (one swizzled half)
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t v_full[kStagesV], v_empty[kStagesV];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done, drain;
+  uint32_t tmem_base;
+};
+
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (1 + kStagesK + kStagesV) + sizeof(Barriers);
+
+// The unit's KV tiles: per block of the item, keys [lo, lo + n) some row of the
+// tile can see, cut into kN-key tiles.  All roles walk the same sequence.
+struct TileWalk {
+  const int32_t* blocks;
+  const int32_t* table;
+  int32_t blk_cnt, bl, max_blocks, kv_len, vis_max;
+  int64_t n_pool;
+  __device__ __forceinline__ int32_t block(int32_t bi, int32_t* lo, int32_t* n, bool* bad) const {
+    const int32_t j = __ldg(blocks + bi);
+    *lo = j * bl;
+    *n = min(min(bl, kv_len - *lo), vis_max - *lo);
+    *bad = false;
+    if (*n <= 0) return -1;
+    const int32_t phys = j < max_blocks ? __ldg(table + j) : -1;
+    if (phys < 0 || phys >= n_pool) {
+      *bad = true;
+      return -1;
+    }
+    return phys;
+  }
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    partial_tc_kernel(PartialArgs a, int32_t tiles_per_item, const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment: the 128-byte swizzle pattern repeats every 8 rows of 128 B.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;
+  uint8_t* sk = smem + kTileBytes;
+  uint8_t* sv = sk + kStagesK * kTileBytes;
+  Barriers* bar = reinterpret_cast<Barriers*>(sv + kStagesV * kTileBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = blockIdx.x;
+  const int32_t rtile = static_cast<int32_t>(u % tiles_per_item);
+  const int32_t kvh = static_cast<int32_t>((u / tiles_per_item) % a.Hkv);
+  const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(tiles_per_item) * a.Hkv));
+
+  const WorkView wv(a.work);
+  const int32_t* it = wv.item(item);
+  const int32_t seq = __ldg(it + kItSeq);
+  const int32_t blk_off = __ldg(it + kItBlockOff), blk_cnt = __ldg(it + kItBlockCnt);
+  const int32_t part_row = __ldg(it + kItPartRow);
+  const int32_t* sqrow = wv.seq(seq);
+  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t G = a.Hq / a.Hkv;
+  const int32_t rows = q_len * G;
+  const int32_t r0 = rtile * kM;
+  if (r0 >= rows) return;  // uniform over the CTA
+  if (part_row < 0 || static_cast<int64_t>(part_row) + q_len > a.part_rows) {
+    if (threadIdx.x == 0) atomicOr(a.status, 2u);
+    return;
+  }
+  const int32_t n_rows = min(kM, rows - r0);
+  const int32_t vis_first = visible_keys(q_len, kv_len, r0 / G, a.causal);
+  const int32_t vis_last = visible_keys(q_len, kv_len, (r0 + n_rows - 1) / G, a.causal);
+  const TileWalk walk{wv.blocks() + blk_off, a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq,
+                      blk_cnt, a.block_len, a.max_blocks_per_seq, kv_len, vis_last, a.n_pool_blocks};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar->q_full, 1);
+    for (int s = 0; s < kStagesK; ++s) {
+      ptx::mbar_init(&bar->k_full[s], 1);
+      ptx::mbar_init(&bar->k_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesV; ++s) {
+      ptx::mbar_init(&bar->v_full[s], 1);
+      ptx::mbar_init(&bar->v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bar->s_full[s], 1);
+      ptx::mbar_init(&bar->p_full[s], 4);
+    }
+    ptx::mbar_init(&bar->o_done, 1);
+    ptx::mbar_init(&bar->drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(&bar->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bar->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_q);
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+      ptx::mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
+      const int32_t tok0 = cu_q + r0 / G;
+      ptx::tma_load_3d(sq, &tmap_q, 0, kvh * G, tok0, &bar->q_full);
+      ptx::tma_load_3d(sq + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->q_full);
+      int32_t t = 0;
+      bool ok = true;
+      for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
+        int32_t lo, n;
+        bool bad;
+        const int32_t phys = walk.block(bi, &lo, &n, &bad);
+        if (bad) atomicOr(a.status, 1u);
+        if (phys < 0) continue;
+        for (int32_t off = 0; off < n; off += kN, ++t) {
+          const int32_t tok = phys * a.block_len + off;
+          const int ks = t % kStagesK, vs = t % kStagesV;
+          if (t >= kStagesK && !ptx::mbar_wait(&bar->k_empty[ks], ((t / kStagesK) & 1) ^ 1)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&bar->k_full[ks], kTileBytes);
+          ptx::tma_load_3d(sk + ks * kTileBytes, &tmap_k, 0, kvh, tok, &bar->k_full[ks]);
+          ptx::tma_load_3d(sk + ks * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->k_full[ks]);
+          if (t >= kStagesV && !ptx::mbar_wait(&bar->v_empty[vs], ((t / kStagesV) & 1) ^ 1)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&bar->v_full[vs], kTileBytes);
+          ptx::tma_load_3d(sv + vs * kTileBytes, &tmap_v, 0, kvh, tok, &bar->v_full[vs]);
+          ptx::tma_load_3d(sv + vs * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->v_full[vs]);
+        }
+      }
+      if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
+      // every copy issued has landed before shared memory is released
+      if (!ptx::mbar_wait(&bar->q_full, 0)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, t - kStagesK); v < t; ++v)
+        if (!ptx::mbar_wait(&bar->k_full[v % kStagesK], (v / kStagesK) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, t - kStagesV); v < t; ++v)
+        if (!ptx::mbar_wait(&bar->v_full[v % kStagesV], (v / kStagesV) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA
+    const uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, false, false);
+    const uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, false, true);
+    const uint32_t q_addr = ptx::smem_addr(sq);
+    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
+    // S_t = Q K_t^T into S buffer t % 2
+    auto issue_s = [&](int32_t t) -> bool {
+      const int ks = t % kStagesK;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[ks], (t / kStagesK) & 1))) return false;
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t k_addr = ptx::smem_addr(sk + ks * kTileBytes);
+        const uint32_t d_col = tmem + ((t & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          tc::mma_ss(d_col, tc::smem_desc(q_addr + off, 16, 1024, tc::kSwizzle128B),
+                     tc::smem_desc(k_addr + off, 16, 1024, tc::kSwizzle128B), idesc_qk, kk > 0);
+        }
+        tc::commit(&bar->k_empty[ks]);
+        tc::commit(&bar->s_full[t & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // tile sequence with the valid key count of each tile
+    int32_t t = 0;
+    int32_t bi = 0, off = 0, n = 0;
+    bool have = false;
+    auto next_tile = [&](int32_t* nvalid) -> bool {  // advances to the next tile
+      while (true) {
+        if (have && off + kN < n) {
+          off += kN;
+          *nvalid = min(kN, n - off);
+          return true;
+        }
+        have = false;
+        while (bi < blk_cnt) {
+          int32_t lo;
+          bool bad;
+          const int32_t phys = walk.block(bi++, &lo, &n, &bad);
+          if (phys >= 0) {
+            have = true;
+            off = 0;
+            *nvalid = min(kN, n);
+            return true;
+          }
+        }
+        return false;
+      }
+    };
+    int32_t nv_cur = 0, nv_next = 0;
+    bool has_cur = ok && next_tile(&nv_cur);
+    if (has_cur) ok = issue_s(0);
+    while (has_cur && ok) {
+      const bool has_next = next_tile(&nv_next);
+      if (has_next && !issue_s(t + 1)) { ok = false; break; }
+      // O += P_t V_t
+      const int vs = t % kStagesV;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[t & 1], (t >> 1) & 1) &&
+                                       ptx::mbar_wait(&bar->v_full[vs], (t / kStagesV) & 1))) { ok = false; break; }
+      tc::fence_after_sync();
+      uint8_t* vtile = sv + vs * kTileBytes;
+      const int ksteps = (nv_cur + 15) >> 4;
+      if (nv_cur < ksteps * 16) {
+        // zero the V rows of keys past the end inside the last 16-key step
+        for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
+          uint4* row0 = reinterpret_cast<uint4*>(vtile + r * 128);
+          uint4* row1 = reinterpret_cast<uint4*>(vtile + kHalfBytes + r * 128);
+          const int c = lane & 15;
+          if (c < 8) row0[c] = make_uint4(0, 0, 0, 0); else row1[c - 8] = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        const uint32_t v_addr = ptx::smem_addr(vtile);
+        const uint32_t p_col = tmem + ((t & 1) ? kColS1 : kColS0);
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc::mma_ts(tmem + kColO, p_col + 8 * kk, tc::smem_desc(v_addr + kk * 2048, kHalfBytes, 1024, tc::kSwizzle128B),
+                     idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bar->v_empty[vs]);
+        tc::commit(&bar->o_done);
+      }
+      __syncwarp();
+      ++t;
+      has_cur = has_next;
+      nv_cur = nv_next;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    // all MMAs issued by this warp have completed before TMEM is released
+    if (lane == 0) tc::commit(&bar->drain);
+    __syncwarp();
+    if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+  } else {
+    // --------------------------------------------------- softmax + epilogue
+    const int row = warp * 32 + lane;  // == TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool row_valid = row < n_rows;
+    const int32_t my_vis = row_valid ? visible_keys(q_len, kv_len, (r0 + row) / G, a.causal) : 0;
+    const float c = a.scale * kLog2e;  // scores -> base-2 exponent
+    float m_used = -INFINITY;          // raw-score max the exponentials are taken against
+    float l = 0.f;
+    int32_t t = 0;
+    bool ok = true;
+    for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
+      int32_t lo, n;
+      bool bad;
+      const int32_t phys = walk.block(bi, &lo, &n, &bad);
+      if (phys < 0) continue;
+      for (int32_t off = 0; off < n; off += kN, ++t) {
+        const int32_t pos0 = lo + off;
+        const int32_t nvalid = min(kN, n - off);
+        // waits and TMEM accesses stay warp-uniform (tcgen05.ld/st are warp-collective)
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1))) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t s_addr = lane_addr + ((t & 1) ? kColS1 : kColS0);
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(s_addr + 32 * q4, sr[q4]);
+        tc::tmem_ld_wait();
+        // visible keys of this row inside the tile: [0, lim)
+        const int32_t lim = min(nvalid, my_vis - pos0);
+        const bool whole = pos0 + kN <= vis_first && nvalid == kN;  // uniform: no masking needed
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float s = __uint_as_float(sr[q4][i]);
+            if (!whole && 32 * q4 + i >= lim) s = -INFINITY;
+            sr[q4][i] = __float_as_uint(s);
+            mx = fmaxf(mx, s);
+          }
+        bool need = false;
+        float alpha = 1.f;
+        if (mx != -INFINITY) {
+          if (m_used == -INFINITY) {
+            m_used = mx;  // nothing accumulated yet: O and l are zero
+          } else if ((mx - m_used) * c > kRescaleThreshold) {
+            need = true;
+            alpha = fast_exp2((m_used - mx) * c);
+            m_used = mx;
+            l *= alpha;
+          }
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // O must hold P_{t-1} V_{t-1} before it is rescaled (need implies t > 0)
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) { ok = false; break; }
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t orr[32];
+            tc::tmem_ld32(lane_addr + kColO + 32 * q4, orr);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tc::tmem_st32(lane_addr + kColO + 32 * q4, orr);
+          }
+          tc::tmem_st_wait();
+        }
+        const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
+        float sum = 0.f;
+        uint32_t pw[2][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[q4][2 * i]), c, -mc));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[q4][2 * i + 1]), c, -mc));
+            sum += p0 + p1;
+            pw[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16(p0, p1);
+          }
+        l += sum;
+        const uint32_t p_addr = lane_addr + ((t & 1) ? kColS1 : kColS0);
+        tc::tmem_st32(p_addr, pw[0]);
+        tc::tmem_st32(p_addr + 32, pw[1]);
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bar->p_full[t & 1]);
+      }
+    }
+    // epilogue: O / l and the log-sum-exp of this row
+    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) ok = false;
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    tc::fence_after_sync();
+    const int64_t orow = static_cast<int64_t>(part_row + (r0 + row) / G) * a.Hq + kvh * G + (r0 + row) % G;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t orr[32];
+      if (t > 0) {
+        tc::tmem_ld32(lane_addr + kColO + 32 * q4, orr);
+        tc::tmem_ld_wait();
+      }
+      if (row_valid) {
+        float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kD + 32 * q4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (t > 0 && l > 0.f)
+            v = make_float4(__uint_as_float(orr[4 * i]) * inv, __uint_as_float(orr[4 * i + 1]) * inv,
+                            __uint_as_float(orr[4 * i + 2]) * inv, __uint_as_float(orr[4 * i + 3]) * inv);
+          dst[i] = v;
+        }
+      }
+    }
+    if (row_valid) a.lse_part[orow] = l > 0.f ? (m_used * c + __log2f(l)) * kLn2 : -INFINITY;
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool tc_supports(const PartialArgs& a) {
+  if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
+  const int32_t G = a.Hq / a.Hkv;
+  return G >= 1 && G <= kM && kM % G == 0 && a.block_len % kN == 0 &&
+         static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
+}
+
+int launch_partial_tc(const PartialArgs& a, cudaStream_t stream) {
+  const int32_t G = a.Hq / a.Hkv;
+  const int32_t tiles = (a.max_q_len * G + kM - 1) / kM;
+  const int64_t grid = static_cast<int64_t>(tiles) * a.Hkv * a.n_items;
+  if (grid == 0) return SPLITKV_OK;
+  if (grid > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many work units");
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
+    const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hq) * kD * 2ull};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kM / G)};
+    const int st = encode_bf16_3d(&tq, a.q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != SPLITKV_OK) return st;
+  }
+  {
+    const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.n_pool_blocks) * a.block_len};
+    const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hkv) * kD * 2ull};
+    const uint32_t box[3] = {64, 1, kN};
+    int st = encode_bf16_3d(&tk, a.k_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != SPLITKV_OK) return st;
+    st = encode_bf16_3d(&tv, a.v_pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != SPLITKV_OK) return st;
+  }
+  cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "tc smem attribute: %s", cudaGetErrorString(e));
+  partial_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, tiles, tq, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));
+  return SPLITKV_OK;
+}
+
 }  // namespace splitkv
