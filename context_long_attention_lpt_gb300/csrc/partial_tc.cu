@@ -353,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold P_{t-1} V_{t-1} before it is rescaled (need implies t > 0)
+          // O must hold P_{t-1} V_{t-1} before it is rescaled (need implies t > 0);
+          // PV_{t-2} was observed before P_{t-1} was published, so this wait is exact
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) { ok = false; break; }
           tc::fence_after_sync();
 #pragma unroll 1
@@ -385,11 +386,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st32(p_addr + 32, pw[1]);
         tc::tmem_st_wait();
         tc::fence_before_sync();
+        // Observe every o_done phase in order, before P_t is published: a parity
+        // wait is only unambiguous while the barrier is at most one phase away,
+        // and PV_t cannot start before P_t exists.  PV_{t-1} was issued when
+        // P_{t-1} landed, so it has normally finished by now.
+        if (t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) {
+          ok = false;
+          ++t;
+          break;
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bar->p_full[t & 1]);
       }
     }
-    // epilogue: O / l and the log-sum-exp of this row
+    // epilogue: O / l and the log-sum-exp of this row (PV_{t-2} observed before P_{t-1})
     if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) ok = false;
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     tc::fence_after_sync();

@@ -46,6 +46,21 @@ def test_small_cases_every_element(name, kernel):
     o_ref, l_ref = full_reference(inp)
     eo, el = max_errors(out, lse, o_ref, l_ref)
     assert_close(w, eo, el, f"{name}/{K.KERNEL_NAMES.get(run.kernel_used())}")
+    assert K.splitkv_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tensor_core_few_tile_items(seed):
+    """Items of one or two 128-key tiles, partial query tiles and a ragged last block:
+    the pipeline's start-up and drain paths of the tensor-core kernel, repeated."""
+    rng = np.random.default_rng(seed)
+    w = wl.custom("shortq", causal=bool(seed % 2), q_len=int(rng.integers(1, 70)),
+                  context=int(rng.integers(200, 1500)), block_len=128, n_shards=int(rng.integers(2, 9)),
+                  seed=100 + seed)
+    inp, run, out, lse = run_cuda(w, kernel=K.KERNEL_TC)
+    eo, el = max_errors(out, lse, *full_reference(inp))
+    assert_close(w, eo, el, f"seed {seed}")
+    assert K.splitkv_device_status(clear=True) == 0
 
 
 @pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
