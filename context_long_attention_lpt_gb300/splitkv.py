@@ -34,6 +34,9 @@ _SIGNATURES = {
                                              _i32, _i32, _i32, _i32, _f32, _i32, _i32, _p, _p, _i64,
                                              _i32, _p]),
     "splitkv_merge": (ctypes.c_int, [_p, _p, _i64, _p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]),
+    "splitkv_attention_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i64, _i32, _i32, _i32,
+                                                  _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i64, _p,
+                                                  _p, _p]),
     "splitkv_device_status": (ctypes.c_int, [_p, _i32]),
     "splitkv_last_error": (ctypes.c_char_p, []),
 }
@@ -182,6 +185,26 @@ def splitkv_merge(o_part, lse_part, work, B, total_q, out, lse_out, stream=None)
         o_part.data_ptr(), lse_part.data_ptr(), o_part.shape[0], work.data_ptr(), B, total_q, hq, d,
         _dtype_code(out),
         out.data_ptr(), lse_out.data_ptr(), _stream_handle(stream)))
+
+
+def splitkv_attention_noalloc(q, k_pool, v_pool, block_table, work_host, n_items, B, total_q, max_q_len,
+                              block_len, scale, causal, part_rows, out, lse_out, stream=None):
+    """Partial attention + merge with the library's fixed scratch array; work_host is the
+    numpy int32 descriptor from splitkv_build_work.  out [total_q, Hq, d], lse_out fp32 [total_q, Hq]."""
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
+                    ("out", out), ("lse_out", lse_out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    work = _np(work_host, np.int32)
+    _, hq, d = q.shape
+    n_pool, bl, hkv, _ = k_pool.shape
+    if bl != block_len:
+        raise ValueError("k_pool shape does not match block_len")
+    _check("splitkv_attention_noalloc", lib().splitkv_attention_noalloc(
+        q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), n_pool, block_table.data_ptr(),
+        block_table.shape[1], _ptr(work), work.size, n_items, B, total_q, max_q_len, hq, hkv, d, block_len,
+        float(scale), int(bool(causal)), _dtype_code(q), part_rows, out.data_ptr(), lse_out.data_ptr(),
+        _stream_handle(stream)))
 
 
 def splitkv_device_status(clear=False):

@@ -147,6 +147,40 @@ int splitkv_merge(const float* o_part, const float* lse_part, int64_t part_rows,
                   const int32_t* work, int32_t B, int32_t total_q, int32_t Hq, int32_t d,
                   int32_t dtype, void* out, float* lse_out, void* stream);
 
+/* Size in bytes of the fixed device array used by splitkv_attention_noalloc. */
+#define SPLITKV_NOALLOC_SCRATCH_BYTES (64ll << 20)
+
+/* The whole device path (partial attention, then merge) in one call that
+ * allocates nothing - no cudaMalloc, cudaFree or allocating library routine.
+ * The pages have no counterpart to it.  It is for callers that cannot allocate
+ * device memory themselves: plugins inside a host that owns all device memory
+ * through its own arena, loops that must not stall or fail on an allocation,
+ * embedders that only pass buffers they already own.  The caller passes the
+ * inputs and outputs of splitkv_attn_partial / splitkv_merge, and the work
+ * descriptor as the HOST buffer from splitkv_build_work (work_words words); the
+ * descriptor copy and the partials live in one fixed array of
+ * SPLITKV_NOALLOC_SCRATCH_BYTES bytes declared by the library in device memory,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Needs 4*words + 4*part_rows*Hq*(d+1) bytes (each part rounded up to 256);
+ *     larger problems are rejected with SPLITKV_ERR_CAPACITY before any work.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (each partial row read is written
+ *     first).  Calls whose GPU work overlaps - on different streams, or from
+ *     different host threads - race on the array and give wrong results.
+ *   - A pinned work_host must stay unchanged until the stream has run the copy;
+ *     a pageable one is read before the call returns.
+ * Kernel choice is SPLITKV_KERNEL_AUTO.  Returns 0 or a negative status. */
+int splitkv_attention_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                              int64_t n_pool_blocks, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, const int32_t* work_host,
+                              int64_t work_words, int32_t n_items, int32_t B, int32_t total_q,
+                              int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t d,
+                              int32_t block_len, float scale, int32_t causal, int32_t dtype,
+                              int64_t part_rows, void* out, float* lse_out, void* stream);
+
 /* Reads and optionally clears the device status word: bit 0, a logical block
  * past max_blocks_per_seq or a block-table entry outside the pool was skipped;
  * bit 1, a work item's partial rows fell outside part_rows (item skipped).
