@@ -96,9 +96,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Two fp32 -> bf16x2 (round to nearest even), `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -330,16 +346,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visible keys of this row inside the tile: [0, lim)
         const int32_t lim = min(nvalid, my_vis - pos0);
         const bool whole = pos0 + kN <= vis_first && nvalid == kN;  // uniform: no masking needed
-        float mx = -INFINITY;
+        if (!whole) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * q4 + i >= lim) sr[q4][i] = __float_as_uint(-INFINITY);
+        }
+        // row max: eight independent 3-input max chains, then a small tree
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float s = __uint_as_float(sr[q4][i]);
-            if (!whole && 32 * q4 + i >= lim) s = -INFINITY;
-            sr[q4][i] = __float_as_uint(s);
-            mx = fmaxf(mx, s);
-          }
+          for (int i = 0; i < 32; i += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx8[k] = max3(mx8[k], __uint_as_float(sr[q4][i + 2 * k]), __uint_as_float(sr[q4][i + 2 * k + 1]));
+        float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         bool need = false;
         float alpha = 1.f;
         if (mx != -INFINITY) {
@@ -369,18 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
-        float sum = 0.f;
+        // p = 2^(s*c - m*c) in pairs (packed FMA), row sum in four packed partial sums
+        const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+        float2 sum4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
         uint32_t pw[2][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[q4][2 * i]), c, -mc));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[q4][2 * i + 1]), c, -mc));
-            sum += p0 + p1;
-            pw[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16(p0, p1);
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[q4][2 * i]), __uint_as_float(sr[q4][2 * i + 1])),
+                                        c2, nmc2);
+            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            sum4[i & 3] = add2(sum4[i & 3], pp);
+            pw[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16(pp.x, pp.y);
           }
-        l += sum;
+        const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]);
+        const float2 s4 = add2(s01, s23);
+        l += s4.x + s4.y;
         const uint32_t p_addr = lane_addr + ((t & 1) ? kColS1 : kColS0);
         tc::tmem_st32(p_addr, pw[0]);
         tc::tmem_st32(p_addr + 32, pw[1]);
