@@ -6,30 +6,33 @@
 // shard's partial (O_i, L_i) of the Split-KV card's local attention step
 // ("Timeline": keys and values stay local; only a query-sized result leaves).
 //
-// One CTA = one (work item, K/V head, tile of 128 query rows); row r of the
-// tile is token r / G, query head kvh*G + r % G, so the G heads sharing a K/V
-// head share every K/V tile.  Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue: thread i owns row i (TMEM lane i);
-//   warp 4     TMA producer: Q once, then K and V tiles of 128 keys from the
-//              paged pool (3-D maps over [tokens, Hkv, d], 128-byte swizzle,
-//              two 64-column halves per tile) into kStagesK / kStagesV rings;
-//   warp 5     TMEM allocation and MMA issue (one elected lane).
-// Per KV tile j:  S_j = Q K_j^T     tcgen05.mma kind::f16, M=N=128, fp32 in
-//                                   TMEM (two S buffers, alternating);
-//                 softmax_j         rows read S_j with tcgen05.ld, keep a
-//                                   running max/sum in base 2, write
-//                                   P_j = exp2(s*c - m) as bf16 into the first
-//                                   64 columns of S_j's buffer (tcgen05.st);
-//                 O += P_j V_j      tcgen05.mma with A = P_j from TMEM and
-//                                   B = V_j (MN-major) from shared memory.
-// The MMA warp issues S_{j+1} before waiting for P_j, so the tensor cores
-// compute the next scores while the softmax warps work.  The running max is
-// only moved (and O rescaled through TMEM) when it grows by more than 2^8, so
-// P stays <= 256 and the common tile needs no O traffic.
+// One CTA = one (work item, K/V head, 256 query rows) unit, split into two
+// 128-row query tiles A and B that share every K/V tile.  Row r of the unit is
+// token r / G, query head kvh*G + r % G.  Warp roles (384 threads, three
+// warpgroups; the softmax groups take 232 registers a thread, the third 40):
+//   warps 0-3  softmax + epilogue of tile A: thread i owns row i (TMEM lane i);
+//   warps 4-7  the same for tile B;
+//   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//              from the paged pool (3-D maps over [tokens, Hkv, d], 128-byte
+//              swizzle, two 64-column halves per tile) into two-stage rings;
+//   warp 9     TMEM allocation and MMA issue (one elected lane);
+//   warps 10-11 idle (they complete the third warpgroup).
+// TMEM (512 columns): S_A | O_A | S_B | O_B, 128 fp32 columns each.
+// Per KV tile j and query tile X:
+//   S_X = Q_X K_j^T      tcgen05.mma kind::f16, M = N = 128, fp32 in TMEM;
+//   softmax_X            rows read S_X with tcgen05.ld, keep a running max and
+//                        sum in base 2, and write P_X = exp2(s*c - m) as bf16
+//                        into the first 64 columns of S_X (tcgen05.st);
+//   O_X += P_X V_j       tcgen05.mma with A = P_X from TMEM, B = V_j (MN-major).
+// The tensor pipe runs S_A, S_B, PV_A, S_A', PV_B, S_B', ...: while one query
+// tile's softmax runs, the other tile's MMAs keep the tensor cores busy.  The
+// running max is only moved (and O rescaled through TMEM) when it grows by
+// more than 2^8, so P stays <= 256 and the common tile needs no O traffic.
 //
 // Keys past the sequence end (pool slots that may hold anything) get score
 // -inf, and their V rows inside the last 16-key MMA step are zeroed in shared
-// memory before the P.V MMA, so they contribute exactly nothing.
+// memory before the P.V MMAs, so they contribute exactly nothing.  Every wait
+// has a time limit; on expiry the status word gets bit 2 and the CTA unwinds.
 
 #include <cmath>
 
@@ -44,32 +47,40 @@ namespace splitkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kM = 128;   // query rows per CTA
-constexpr int kN = 128;   // keys per tile
-constexpr int kStagesK = 2;
-constexpr int kStagesV = 2;
-constexpr int kThreads = 192;
-constexpr uint32_t kHalfBytes = kN * 64 * 2;   // 128 rows x 64 bf16 (one swizzled half)
+constexpr int kMT = 128;      // rows per query tile
+constexpr int kM = 2 * kMT;   // rows per CTA
+constexpr int kN = 128;       // keys per KV tile
+constexpr int kStages = 2;    // K and V ring depth
+constexpr int kThreads = 384;
+// Register split: launched at 168 a thread (384 x 168 = 64512), the two softmax
+// warpgroups grow to 232 and the producer / MMA warpgroup shrinks to 40:
+// 2 x 128 x 232 + 128 x 40 = 64512.
+constexpr int kRegsSoftmax = 232, kRegsOther = 40;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
+// TMEM columns of query tile x: scores (P aliases their first 64) and output.
+__host__ __device__ constexpr uint32_t col_s(int x) { return x ? 256u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return x ? 384u : 128u; }
+
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[kStagesK], k_empty[kStagesK];
-  uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done, drain;
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
+  uint64_t drain;
   uint32_t tmem_base;
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (1 + kStagesK + kStagesV) + sizeof(Barriers);
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (2 + 2 * kStages) + sizeof(Barriers);
 
 // The unit's KV tiles: per block of the item, keys [lo, lo + n) some row of the
-// tile can see, cut into kN-key tiles.  All roles walk the same sequence.
+// unit can see, cut into kN-key tiles.  All roles walk the same sequence.
 struct TileWalk {
   const int32_t* blocks;
   const int32_t* table;
@@ -118,21 +129,21 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    partial_tc_kernel(PartialArgs a, int32_t tiles_per_item, const __grid_constant__ CUtensorMap tmap_q,
+    partial_tc_kernel(PartialArgs a, int32_t units_per_item, const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the 128-byte swizzle pattern repeats every 8 rows of 128 B.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem;
-  uint8_t* sk = smem + kTileBytes;
-  uint8_t* sv = sk + kStagesK * kTileBytes;
-  Barriers* bar = reinterpret_cast<Barriers*>(sv + kStagesV * kTileBytes);
+  uint8_t* sq = smem;                       // Q_A, Q_B
+  uint8_t* sk = smem + 2 * kTileBytes;      // K ring
+  uint8_t* sv = sk + kStages * kTileBytes;  // V ring
+  Barriers* bar = reinterpret_cast<Barriers*>(sv + kStages * kTileBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = blockIdx.x;
-  const int32_t rtile = static_cast<int32_t>(u % tiles_per_item);
-  const int32_t kvh = static_cast<int32_t>((u / tiles_per_item) % a.Hkv);
-  const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(tiles_per_item) * a.Hkv));
+  const int32_t utile = static_cast<int32_t>(u % units_per_item);
+  const int32_t kvh = static_cast<int32_t>((u / units_per_item) % a.Hkv);
+  const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(units_per_item) * a.Hkv));
 
   const WorkView wv(a.work);
   const int32_t* it = wv.item(item);
@@ -143,37 +154,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
-  const int32_t r0 = rtile * kM;
+  const int32_t r0 = utile * kM;
   if (r0 >= rows) return;  // uniform over the CTA
   if (part_row < 0 || static_cast<int64_t>(part_row) + q_len > a.part_rows) {
     if (threadIdx.x == 0) atomicOr(a.status, 2u);
     return;
   }
   const int32_t n_rows = min(kM, rows - r0);
-  const int32_t vis_first = visible_keys(q_len, kv_len, r0 / G, a.causal);
+  const bool has_b = n_rows > kMT;  // uniform: the second query tile holds rows
   const int32_t vis_last = visible_keys(q_len, kv_len, (r0 + n_rows - 1) / G, a.causal);
   const TileWalk walk{wv.blocks() + blk_off, a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq,
                       blk_cnt, a.block_len, a.max_blocks_per_seq, kv_len, vis_last, a.n_pool_blocks};
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar->q_full, 1);
-    for (int s = 0; s < kStagesK; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bar->k_full[s], 1);
       ptx::mbar_init(&bar->k_empty[s], 1);
-    }
-    for (int s = 0; s < kStagesV; ++s) {
       ptx::mbar_init(&bar->v_full[s], 1);
       ptx::mbar_init(&bar->v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&bar->s_full[s], 1);
-      ptx::mbar_init(&bar->p_full[s], 4);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&bar->s_full[x], 1);
+      ptx::mbar_init(&bar->p_full[x], 4);
+      ptx::mbar_init(&bar->o_done[x], 1);
     }
-    ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&bar->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -182,16 +191,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_base;
 
-  if (warp == 4) {
+  if (warp >= 8) {
+  // Each role's code sits under its own register-budget change, so the
+  // compiler sizes every role for the budget it runs with.
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tmap_q);
       ptx::prefetch_tmap(&tmap_k);
       ptx::prefetch_tmap(&tmap_v);
-      ptx::mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
-      const int32_t tok0 = cu_q + r0 / G;
-      ptx::tma_load_3d(sq, &tmap_q, 0, kvh * G, tok0, &bar->q_full);
-      ptx::tma_load_3d(sq + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->q_full);
+      ptx::mbar_arrive_expect_tx(&bar->q_full, (has_b ? 2 : 1) * kTileBytes);
+      for (int x = 0; x < (has_b ? 2 : 1); ++x) {
+        const int32_t tok0 = cu_q + (r0 + x * kMT) / G;
+        ptx::tma_load_3d(sq + x * kTileBytes, &tmap_q, 0, kvh * G, tok0, &bar->q_full);
+        ptx::tma_load_3d(sq + x * kTileBytes + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->q_full);
+      }
       int32_t t = 0;
       bool ok = true;
       for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
@@ -202,56 +217,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (phys < 0) continue;
         for (int32_t off = 0; off < n; off += kN, ++t) {
           const int32_t tok = phys * a.block_len + off;
-          const int ks = t % kStagesK, vs = t % kStagesV;
-          if (t >= kStagesK && !ptx::mbar_wait(&bar->k_empty[ks], ((t / kStagesK) & 1) ^ 1)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&bar->k_full[ks], kTileBytes);
-          ptx::tma_load_3d(sk + ks * kTileBytes, &tmap_k, 0, kvh, tok, &bar->k_full[ks]);
-          ptx::tma_load_3d(sk + ks * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->k_full[ks]);
-          if (t >= kStagesV && !ptx::mbar_wait(&bar->v_empty[vs], ((t / kStagesV) & 1) ^ 1)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&bar->v_full[vs], kTileBytes);
-          ptx::tma_load_3d(sv + vs * kTileBytes, &tmap_v, 0, kvh, tok, &bar->v_full[vs]);
-          ptx::tma_load_3d(sv + vs * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->v_full[vs]);
+          const int s = t % kStages;
+          const uint32_t ph = ((t / kStages) & 1) ^ 1;
+          if (t >= kStages && !ptx::mbar_wait(&bar->k_empty[s], ph)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&bar->k_full[s], kTileBytes);
+          ptx::tma_load_3d(sk + s * kTileBytes, &tmap_k, 0, kvh, tok, &bar->k_full[s]);
+          ptx::tma_load_3d(sk + s * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->k_full[s]);
+          if (t >= kStages && !ptx::mbar_wait(&bar->v_empty[s], ph)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&bar->v_full[s], kTileBytes);
+          ptx::tma_load_3d(sv + s * kTileBytes, &tmap_v, 0, kvh, tok, &bar->v_full[s]);
+          ptx::tma_load_3d(sv + s * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->v_full[s]);
         }
       }
       if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
       // every copy issued has landed before shared memory is released
       if (!ptx::mbar_wait(&bar->q_full, 0)) atomicOr(a.status, ptx::kStatusTimeout);
-      for (int32_t v = max(0, t - kStagesK); v < t; ++v)
-        if (!ptx::mbar_wait(&bar->k_full[v % kStagesK], (v / kStagesK) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
-      for (int32_t v = max(0, t - kStagesV); v < t; ++v)
-        if (!ptx::mbar_wait(&bar->v_full[v % kStagesV], (v / kStagesV) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------------ MMA
-    const uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, false, false);
-    const uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, false, true);
-    const uint32_t q_addr = ptx::smem_addr(sq);
-    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
-    // S_t = Q K_t^T into S buffer t % 2
-    auto issue_s = [&](int32_t t) -> bool {
-      const int ks = t % kStagesK;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[ks], (t / kStagesK) & 1))) return false;
-      tc::fence_after_sync();
-      if (lane == 0) {
-        const uint32_t k_addr = ptx::smem_addr(sk + ks * kTileBytes);
-        const uint32_t d_col = tmem + ((t & 1) ? kColS1 : kColS0);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          tc::mma_ss(d_col, tc::smem_desc(q_addr + off, 16, 1024, tc::kSwizzle128B),
-                     tc::smem_desc(k_addr + off, 16, 1024, tc::kSwizzle128B), idesc_qk, kk > 0);
-        }
-        tc::commit(&bar->k_empty[ks]);
-        tc::commit(&bar->s_full[t & 1]);
+      for (int32_t v = max(0, t - kStages); v < t; ++v) {
+        if (!ptx::mbar_wait(&bar->k_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+        if (!ptx::mbar_wait(&bar->v_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
       }
-      __syncwarp();
-      return true;
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
+    const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
+    const uint32_t q_addr = ptx::smem_addr(sq);
+    const int nx = has_b ? 2 : 1;
+    // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
+    auto issue_s = [&](int x, int32_t t) {
+      const uint32_t k_addr = ptx::smem_addr(sk + (t % kStages) * kTileBytes);
+      const uint32_t qx = q_addr + x * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        tc::mma_ss(tmem + col_s(x), tc::smem_desc(qx + off, 16, 1024, tc::kSwizzle128B),
+                   tc::smem_desc(k_addr + off, 16, 1024, tc::kSwizzle128B), idesc_qk, kk > 0);
+      }
+      tc::commit(&bar->s_full[x]);
     };
     // tile sequence with the valid key count of each tile
-    int32_t t = 0;
     int32_t bi = 0, off = 0, n = 0;
     bool have = false;
-    auto next_tile = [&](int32_t* nvalid) -> bool {  // advances to the next tile
+    auto next_tile = [&](int32_t* nvalid) -> bool {
       while (true) {
         if (have && off + kN < n) {
           off += kN;
@@ -273,40 +280,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
     };
+    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
     int32_t nv_cur = 0, nv_next = 0;
     bool has_cur = ok && next_tile(&nv_cur);
-    if (has_cur) ok = issue_s(0);
+    int32_t t = 0;
+    if (has_cur) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
+      tc::fence_after_sync();
+      if (ok && lane == 0) {
+        for (int x = 0; x < nx; ++x) issue_s(x, 0);
+        tc::commit(&bar->k_empty[0]);
+      }
+      __syncwarp();
+    }
     while (has_cur && ok) {
       const bool has_next = next_tile(&nv_next);
-      if (has_next && !issue_s(t + 1)) { ok = false; break; }
-      // O += P_t V_t
-      const int vs = t % kStagesV;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[t & 1], (t >> 1) & 1) &&
-                                       ptx::mbar_wait(&bar->v_full[vs], (t / kStagesV) & 1))) { ok = false; break; }
-      tc::fence_after_sync();
+      const int vs = t % kStages;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1))) { ok = false; break; }
       uint8_t* vtile = sv + vs * kTileBytes;
       const int ksteps = (nv_cur + 15) >> 4;
       if (nv_cur < ksteps * 16) {
         // zero the V rows of keys past the end inside the last 16-key step
         for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
-          uint4* row0 = reinterpret_cast<uint4*>(vtile + r * 128);
-          uint4* row1 = reinterpret_cast<uint4*>(vtile + kHalfBytes + r * 128);
-          const int c = lane & 15;
-          if (c < 8) row0[c] = make_uint4(0, 0, 0, 0); else row1[c - 8] = make_uint4(0, 0, 0, 0);
+          const int cc = lane & 15;
+          uint4* dst = reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128) + (cc & 7);
+          *dst = make_uint4(0, 0, 0, 0);
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        const uint32_t v_addr = ptx::smem_addr(vtile);
-        const uint32_t p_col = tmem + ((t & 1) ? kColS1 : kColS0);
-        for (int kk = 0; kk < ksteps; ++kk)
-          tc::mma_ts(tmem + kColO, p_col + 8 * kk, tc::smem_desc(v_addr + kk * 2048, kHalfBytes, 1024, tc::kSwizzle128B),
-                     idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bar->v_empty[vs]);
-        tc::commit(&bar->o_done);
+      const uint32_t v_addr = ptx::smem_addr(vtile);
+      if (has_next &&
+          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
+        ok = false;
+        break;
       }
-      __syncwarp();
+      for (int x = 0; x < nx; ++x) {
+        // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[x], t & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc::mma_ts(tmem + col_o(x), tmem + col_s(x) + 8 * kk,
+                       tc::smem_desc(v_addr + kk * 2048, kHalfBytes, 1024, tc::kSwizzle128B), idesc_pv,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&bar->o_done[x]);
+          if (x == nx - 1) tc::commit(&bar->v_empty[vs]);
+          if (has_next) {
+            issue_s(x, t + 1);
+            if (x == nx - 1) tc::commit(&bar->k_empty[(t + 1) % kStages]);
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
       ++t;
       has_cur = has_next;
       nv_cur = nv_next;
@@ -316,12 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+  }
   } else {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+  if (warp < 4 || has_b) {
     // --------------------------------------------------- softmax + epilogue
-    const int row = warp * 32 + lane;  // == TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int x = warp >> 2;           // query tile
+    const int wq = warp & 3;           // TMEM lane quarter
+    const int32_t row = x * kMT + wq * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t s_addr = lane_addr + col_s(x), o_addr = lane_addr + col_o(x);
     const bool row_valid = row < n_rows;
     const int32_t my_vis = row_valid ? visible_keys(q_len, kv_len, (r0 + row) / G, a.causal) : 0;
+    // every row of this query tile sees the keys below vis_first (uniform over the tile)
+    const int32_t vis_first = visible_keys(q_len, kv_len, (r0 + x * kMT) / G, a.causal);
     const float c = a.scale * kLog2e;  // scores -> base-2 exponent
     float m_used = -INFINITY;          // raw-score max the exponentials are taken against
     float l = 0.f;
@@ -336,9 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t pos0 = lo + off;
         const int32_t nvalid = min(kN, n - off);
         // waits and TMEM accesses stay warp-uniform (tcgen05.ld/st are warp-collective)
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1))) { ok = false; break; }
         tc::fence_after_sync();
-        const uint32_t s_addr = lane_addr + ((t & 1) ? kColS1 : kColS0);
         uint32_t sr[4][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(s_addr + 32 * q4, sr[q4]);
@@ -364,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mx8[k] = max3(mx8[k], __uint_as_float(sr[q4][i + 2 * k]), __uint_as_float(sr[q4][i + 2 * k + 1]));
-        float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         bool need = false;
         float alpha = 1.f;
         if (mx != -INFINITY) {
@@ -380,16 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           // O must hold P_{t-1} V_{t-1} before it is rescaled (need implies t > 0);
           // PV_{t-2} was observed before P_{t-1} was published, so this wait is exact
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) { ok = false; break; }
           tc::fence_after_sync();
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t orr[32];
-            tc::tmem_ld32(lane_addr + kColO + 32 * q4, orr);
+            tc::tmem_ld32(o_addr + 32 * q4, orr);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tc::tmem_st32(lane_addr + kColO + 32 * q4, orr);
+            tc::tmem_st32(o_addr + 32 * q4, orr);
           }
           tc::tmem_st_wait();
         }
@@ -404,35 +441,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[q4][2 * i]), __uint_as_float(sr[q4][2 * i + 1])),
-                                        c2, nmc2);
-            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            const float2 xx = ptx::ffma2(make_float2(__uint_as_float(sr[q4][2 * i]), __uint_as_float(sr[q4][2 * i + 1])),
+                                         c2, nmc2);
+            const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
             sum4[i & 3] = add2(sum4[i & 3], pp);
             pw[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16(pp.x, pp.y);
           }
-        const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]);
-        const float2 s4 = add2(s01, s23);
+        const float2 s4 = add2(add2(sum4[0], sum4[1]), add2(sum4[2], sum4[3]));
         l += s4.x + s4.y;
-        const uint32_t p_addr = lane_addr + ((t & 1) ? kColS1 : kColS0);
-        tc::tmem_st32(p_addr, pw[0]);
-        tc::tmem_st32(p_addr + 32, pw[1]);
+        tc::tmem_st32(s_addr, pw[0]);
+        tc::tmem_st32(s_addr + 32, pw[1]);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         // Observe every o_done phase in order, before P_t is published: a parity
         // wait is only unambiguous while the barrier is at most one phase away,
-        // and PV_t cannot start before P_t exists.  PV_{t-1} was issued when
-        // P_{t-1} landed, so it has normally finished by now.
-        if (t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) {
+        // and PV_t cannot start before P_t exists.
+        if (t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) {
           ok = false;
           ++t;
           break;
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar->p_full[t & 1]);
+        if (lane == 0) ptx::mbar_arrive(&bar->p_full[x]);
       }
     }
     // epilogue: O / l and the log-sum-exp of this row (PV_{t-2} observed before P_{t-1})
-    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (t - 1) & 1))) ok = false;
+    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) ok = false;
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     tc::fence_after_sync();
     const int64_t orow = static_cast<int64_t>(part_row + (r0 + row) / G) * a.Hq + kvh * G + (r0 + row) % G;
@@ -441,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t orr[32];
       if (t > 0) {
-        tc::tmem_ld32(lane_addr + kColO + 32 * q4, orr);
+        tc::tmem_ld32(o_addr + 32 * q4, orr);
         tc::tmem_ld_wait();
       }
       if (row_valid) {
@@ -458,10 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (row_valid) a.lse_part[orow] = l > 0.f ? (m_used * c + __log2f(l)) * kLn2 : -INFINITY;
   }
+  }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -472,21 +507,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool tc_supports(const PartialArgs& a) {
   if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
   const int32_t G = a.Hq / a.Hkv;
-  return G >= 1 && G <= kM && kM % G == 0 && a.block_len % kN == 0 &&
+  return G >= 1 && G <= kMT && kMT % G == 0 && a.block_len % kN == 0 &&
          static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
 }
 
 int launch_partial_tc(const PartialArgs& a, cudaStream_t stream) {
   const int32_t G = a.Hq / a.Hkv;
-  const int32_t tiles = (a.max_q_len * G + kM - 1) / kM;
-  const int64_t grid = static_cast<int64_t>(tiles) * a.Hkv * a.n_items;
+  const int32_t units = (a.max_q_len * G + kM - 1) / kM;
+  const int64_t grid = static_cast<int64_t>(units) * a.Hkv * a.n_items;
   if (grid == 0) return SPLITKV_OK;
   if (grid > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many work units");
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
     const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hq) * kD * 2ull};
-    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kM / G)};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kMT / G)};
     const int st = encode_bf16_3d(&tq, a.q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != SPLITKV_OK) return st;
   }
@@ -502,7 +537,7 @@ int launch_partial_tc(const PartialArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "tc smem attribute: %s", cudaGetErrorString(e));
-  partial_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, tiles, tq, tk, tv);
+  partial_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, units, tq, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));
   return SPLITKV_OK;
