@@ -9,7 +9,7 @@
 // One CTA = one (work item, K/V head, 256 query rows) unit, split into two
 // 128-row query tiles A and B that share every K/V tile.  Row r of the unit is
 // token r / G, query head kvh*G + r % G.  Warp roles (384 threads, three
-// warpgroups; the softmax groups take 232 registers a thread, the third 40):
+// warpgroups; the softmax groups take 224 registers a thread, the third 56):
 //   warps 0-3  softmax + epilogue of tile A: thread i owns row i (TMEM lane i);
 //   warps 4-7  the same for tile B;
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
@@ -53,9 +53,9 @@ constexpr int kN = 128;       // keys per KV tile
 constexpr int kStages = 2;    // K and V ring depth
 constexpr int kThreads = 384;
 // Register split: launched at 168 a thread (384 x 168 = 64512), the two softmax
-// warpgroups grow to 232 and the producer / MMA warpgroup shrinks to 40:
-// 2 x 128 x 232 + 128 x 40 = 64512.
-constexpr int kRegsSoftmax = 232, kRegsOther = 40;
+// warpgroups grow to 224 and the producer / MMA warpgroup shrinks to 56:
+// 2 x 128 x 224 + 128 x 56 = 64512 (per SM sub-partition 224 + 224 + 56 <= 512).
+constexpr int kRegsSoftmax = 224, kRegsOther = 56;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
@@ -241,17 +241,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
-    const uint32_t q_addr = ptx::smem_addr(sq);
     const int nx = has_b ? 2 : 1;
+    // Descriptors of every operand tile, built once; an MMA only adds an offset.
+    const tc::Desc desc_q0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc desc_k0 = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
+    constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
     // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
     auto issue_s = [&](int x, int32_t t) {
-      const uint32_t k_addr = ptx::smem_addr(sk + (t % kStages) * kTileBytes);
-      const uint32_t qx = q_addr + x * kTileBytes;
+      const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
+      const uint32_t d_col = tmem + col_s(x);
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-        tc::mma_ss(tmem + col_s(x), tc::smem_desc(qx + off, 16, 1024, tc::kSwizzle128B),
-                   tc::smem_desc(k_addr + off, 16, 1024, tc::kSwizzle128B), idesc_qk, kk > 0);
+        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        tc::mma_ss_fast(d_col, desc_q0, qoff + off, desc_k0, koff + off, idesc_qk, kk > 0);
       }
       tc::commit(&bar->s_full[x]);
     };
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
-      const uint32_t v_addr = ptx::smem_addr(vtile);
+      const uint32_t voff = vs * kTile16;
       if (has_next &&
           !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
         ok = false;
@@ -323,10 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         if (lane == 0) {
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc::mma_ts(tmem + col_o(x), tmem + col_s(x) + 8 * kk,
-                       tc::smem_desc(v_addr + kk * 2048, kHalfBytes, 1024, tc::kSwizzle128B), idesc_pv,
-                       (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
+          if (ksteps == kN / 16 && t > 0) {
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk)
+              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
+          } else {
+            for (int kk = 0; kk < ksteps; ++kk)
+              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
+                              (t > 0 || kk > 0) ? 1u : 0u);
+          }
           tc::commit(&bar->o_done[x]);
           if (x == nx - 1) tc::commit(&bar->v_empty[vs]);
           if (has_next) {

@@ -66,6 +66,42 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 
 // ------------------------------------------------------------------ MMA
 
+// Descriptor split into its two 32-bit words.  The start address sits in the
+// low word, so advancing an operand inside shared memory is one 32-bit add of
+// (byte offset >> 4) - no carry can reach bit 14 for addresses below 256 KB.
+struct Desc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc split(uint64_t d) {
+  return Desc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with pre-split descriptors and byte offsets
+// added to their start fields; the fewest instructions per MMA on the issuing
+// thread, whose issue rate bounds the tensor pipe's.
+__device__ __forceinline__ void mma_ss_fast(uint32_t d_tmem, Desc a, uint32_t a_off16, Desc b, uint32_t b_off16,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + a_off16), "r"(a.hi), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] with a pre-split B descriptor.
+__device__ __forceinline__ void mma_ts_fast(uint32_t d_tmem, uint32_t a_tmem, Desc b, uint32_t b_off16,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
