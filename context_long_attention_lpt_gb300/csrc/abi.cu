@@ -1,5 +1,6 @@
 // extern "C" device-side entry points: argument validation, kernel choice, launch.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -52,14 +53,14 @@ extern "C" int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t b
   return pick_kernel(a, SPLITKV_KERNEL_AUTO);
 }
 
-extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
-                                    int64_t n_pool_blocks, const int32_t* block_table,
-                                    int32_t max_blocks_per_seq, const int32_t* work,
-                                    int32_t n_items, int32_t B, int32_t total_q,
-                                    int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t d,
-                                    int32_t block_len, float scale, int32_t causal,
-                                    int32_t dtype, float* o_part, float* lse_part,
-                                    int64_t part_rows, int32_t kernel, void* stream) {
+namespace {
+
+// Validates the arguments shared by the partial-attention entry points and fills `a`.
+int make_partial_args(splitkv::PartialArgs* a, const void* q, const void* k_pool, const void* v_pool,
+                      int64_t n_pool_blocks, const int32_t* block_table, int32_t max_blocks_per_seq,
+                      const int32_t* work, int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len,
+                      int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, float scale, int32_t causal,
+                      int32_t dtype, float* o_part, float* lse_part, int64_t part_rows, int32_t kernel) {
   if (dtype != SPLITKV_F32 && dtype != SPLITKV_BF16)
     return fail(SPLITKV_ERR_INVALID, "dtype must be SPLITKV_F32 or SPLITKV_BF16 (got %d)", dtype);
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
@@ -78,17 +79,15 @@ extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const voi
   if (kernel < SPLITKV_KERNEL_AUTO || kernel > SPLITKV_KERNEL_TC)
     return fail(SPLITKV_ERR_INVALID, "unknown kernel %d", kernel);
   int err = 0;
-  splitkv::PartialArgs a{q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work,
-                         n_items, B, total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal ? 1 : 0,
-                         dtype, o_part, lse_part, part_rows, nullptr};
-  a.status = status_word(&err);
-  if (!a.status) return err;
-  if (n_items == 0) {
-    splitkv::clear_error();
-    return SPLITKV_OK;
-  }
-  const int k = pick_kernel(a, kernel);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  *a = splitkv::PartialArgs{q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work,
+                            n_items, B, total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal ? 1 : 0,
+                            dtype, o_part, lse_part, part_rows, nullptr, 0, nullptr, nullptr, nullptr};
+  a->status = status_word(&err);
+  if (!a->status) return err;
+  return SPLITKV_OK;
+}
+
+int launch_partial(const splitkv::PartialArgs& a, int k, cudaStream_t s) {
   int st = SPLITKV_OK;
   switch (k) {
     case SPLITKV_KERNEL_TC:
@@ -106,6 +105,81 @@ extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const voi
       const cudaError_t e = splitkv::launch_partial_simt(a, s);
       if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "partial launch: %s", cudaGetErrorString(e));
       break;
+    }
+  }
+  return st;
+}
+
+int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
+                                    int64_t n_pool_blocks, const int32_t* block_table,
+                                    int32_t max_blocks_per_seq, const int32_t* work,
+                                    int32_t n_items, int32_t B, int32_t total_q,
+                                    int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t d,
+                                    int32_t block_len, float scale, int32_t causal,
+                                    int32_t dtype, float* o_part, float* lse_part,
+                                    int64_t part_rows, int32_t kernel, void* stream) {
+  splitkv::PartialArgs a;
+  int st = make_partial_args(&a, q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work, n_items, B,
+                             total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal, dtype, o_part, lse_part,
+                             part_rows, kernel);
+  if (st != SPLITKV_OK) return st;
+  if (n_items == 0) {
+    splitkv::clear_error();
+    return SPLITKV_OK;
+  }
+  st = launch_partial(a, pick_kernel(a, kernel), static_cast<cudaStream_t>(stream));
+  if (st != SPLITKV_OK) return st;
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int64_t splitkv_ticket_count(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_q_len < 0)
+    return fail(SPLITKV_ERR_INVALID, "splitkv_ticket_count: bad arguments");
+  splitkv::clear_error();
+  return static_cast<int64_t>(B) * Hkv * std::max<int64_t>(1, div_up(static_cast<int64_t>(max_q_len) * (Hq / Hkv), 256));
+}
+
+extern "C" int splitkv_attn_fused(const void* q, const void* k_pool, const void* v_pool, int64_t n_pool_blocks,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* work,
+                                  int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,
+                                  int32_t Hkv, int32_t d, int32_t block_len, float scale, int32_t causal,
+                                  int32_t dtype, float* o_part, float* lse_part, int64_t part_rows,
+                                  uint32_t* tickets, int64_t n_tickets, void* out, float* lse_out, int32_t kernel,
+                                  void* stream) {
+  splitkv::PartialArgs a;
+  int st = make_partial_args(&a, q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work, n_items, B,
+                             total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal, dtype, o_part, lse_part,
+                             part_rows, kernel);
+  if (st != SPLITKV_OK) return st;
+  if (total_q > 0 && (!out || !lse_out)) return fail(SPLITKV_ERR_INVALID, "null output pointer");
+  const int64_t need = splitkv_ticket_count(B, Hq, Hkv, max_q_len);
+  if (need < 0) return static_cast<int>(need);
+  if (!tickets || n_tickets < need)
+    return fail(SPLITKV_ERR_CAPACITY, "tickets holds %lld counters, needs %lld", (long long)n_tickets, (long long)need);
+  if (n_items == 0) {
+    splitkv::clear_error();
+    return SPLITKV_OK;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int k = pick_kernel(a, kernel);
+  if (k == SPLITKV_KERNEL_DECODE && splitkv::decode_fuses(a)) {
+    a.fused = 1;
+    a.tickets = tickets;
+    a.out = out;
+    a.lse_out = lse_out;
+    st = launch_partial(a, k, s);
+  } else {
+    // kernels without an in-kernel merge: the same two launches as the separate calls
+    st = launch_partial(a, k, s);
+    if (st == SPLITKV_OK) {
+      const cudaError_t e = splitkv::launch_merge(o_part, lse_part, part_rows, work, B, total_q, Hq, d, dtype, out,
+                                                  lse_out, a.status, s);
+      if (e != cudaSuccess) st = fail(SPLITKV_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
     }
   }
   if (st != SPLITKV_OK) return st;

@@ -33,6 +33,12 @@ struct PartialArgs {
   float* lse_part;
   int64_t part_rows;
   unsigned int* status;  // device status word (bit 0: block-table entry out of range)
+  // Fused merge (decode kernel): the last CTA of each (sequence, K/V head) group,
+  // found by an atomic ticket, merges the group's partials into out / lse_out.
+  int32_t fused;
+  uint32_t* tickets;  // one counter per (sequence, K/V head), zero between launches
+  void* out;
+  float* lse_out;
 };
 
 // Each launcher returns cudaSuccess or the launch error.
@@ -43,6 +49,7 @@ int launch_partial_tc(const PartialArgs& a, cudaStream_t stream);
 
 // Shape limits of the specialised kernels (checked before launching them).
 bool decode_supports(const PartialArgs& a);
+bool decode_fuses(const PartialArgs& a);  // the decode kernel can merge in the same launch
 bool tc_supports(const PartialArgs& a);
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int64_t part_rows,

@@ -49,6 +49,7 @@ constexpr uint32_t kTileBytes = kKT * kD * 2;  // one K (or V) tile
 constexpr size_t kSmemBytes = kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) + 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxFusedItems = 2048;  // items of one sequence the in-kernel merge can hold in shared memory
 
 // Tiles of a work item: for each of its blocks the keys [lo, lo + n) that some
 // row of the unit can see, cut into kKT-key tiles.  Producer and consumers
@@ -320,6 +321,71 @@ __global__ void __launch_bounds__(kThreads, 2)
     a.o_part[orow * kD + c] = l > 0.f ? o / l : 0.f;
     if (c == 0) a.lse_part[orow] = l > 0.f ? (mx + log2f(l)) * kLn2 : -INFINITY;
   }
+  if (!a.fused) return;
+
+  // ---- fused merge: the last CTA of this (sequence, K/V head) group merges ----
+  // Every thread publishes its partial rows before the group's ticket is taken
+  // (the usual fence-then-count pattern); no CTA ever waits for another.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  uint32_t* ticket = a.tickets + static_cast<int64_t>(seq) * a.Hkv + kvh;
+  const int32_t p0 = __ldg(wv.seq(seq) + kSqItemPtr), p1 = __ldg(wv.seq(seq + 1) + kSqItemPtr);
+  if (threadIdx.x == 0) {
+    const uint32_t taken = atomicAdd(ticket, 1u);
+    s_last = taken == static_cast<uint32_t>(p1 - p0 - 1);
+    __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // Merge: all LSEs of the group at once, weights per row, then the weighted sum
+  // of the partial rows with independent loads (they sit in L2, just written).
+  const int32_t* seq_items = wv.seq_items();
+  const int32_t n_it = p1 - p0;
+  float* sm_w = reinterpret_cast<float*>(smem);            // [n_it][R] weights
+  int32_t* sm_pr = reinterpret_cast<int32_t*>(sm_w + kMaxFusedItems * R);  // [n_it] partial rows
+  for (int i = threadIdx.x; i < n_it; i += kThreads) sm_pr[i] = __ldg(wv.item(__ldg(seq_items + p0 + i)) + kItPartRow);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_it * rows; i += kThreads) {
+    const int it = i / rows, r = i % rows;
+    sm_w[it * R + r] = __ldcg(a.lse_part + static_cast<int64_t>(sm_pr[it] + r / G) * a.Hq + kvh * G + r % G);
+  }
+  __syncthreads();
+  if (threadIdx.x < rows) {
+    const int r = threadIdx.x;
+    float mx = -INFINITY;
+    for (int it = 0; it < n_it; ++it) mx = fmaxf(mx, sm_w[it * R + r]);
+    float sum = 0.f;
+    for (int it = 0; it < n_it; ++it) {
+      const float e = mx == -INFINITY ? 0.f : exp2f((sm_w[it * R + r] - mx) * kLog2e);
+      sm_w[it * R + r] = e;
+      sum += e;
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int it = 0; it < n_it; ++it) sm_w[it * R + r] *= inv;
+    const int64_t orow = static_cast<int64_t>(cu_q + r / G) * a.Hq + kvh * G + r % G;
+    a.lse_out[orow] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows * (kD / 4); i += kThreads) {
+    const int r = i / (kD / 4), c4 = i % (kD / 4);
+    const int32_t tok = r / G, h = kvh * G + r % G;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int it = 0; it < n_it; ++it) {
+      const float w = sm_w[it * R + r];
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(a.o_part + (static_cast<int64_t>(sm_pr[it] + tok) * a.Hq + h) * kD) + c4);
+      o.x = fmaf(w, x.x, o.x);
+      o.y = fmaf(w, x.y, o.y);
+      o.z = fmaf(w, x.z, o.z);
+      o.w = fmaf(w, x.w, o.w);
+    }
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                            (static_cast<int64_t>(cu_q + tok) * a.Hq + h) * kD) + 2 * c4;
+    dst[0] = __floats2bfloat162_rn(o.x, o.y);
+    dst[1] = __floats2bfloat162_rn(o.z, o.w);
+  }
+  if (threadIdx.x == 0) *ticket = 0u;  // ready for the next launch
 }
 
 template <int R>
@@ -336,6 +402,11 @@ int launch_r(const PartialArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
 }
 
 }  // namespace
+
+// The in-kernel merge keeps one weight per (item, row) of a sequence in the
+// freed stage memory: at most kMaxFusedItems items, i.e. a sequence spread over
+// no more than that many shards (weights + rows take 2048 x (8 + 1) x 4 = 73 KB).
+bool decode_fuses(const PartialArgs& a) { return decode_supports(a) && a.n_items <= kMaxFusedItems; }
 
 bool decode_supports(const PartialArgs& a) {
   if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;

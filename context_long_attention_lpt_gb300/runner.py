@@ -19,7 +19,7 @@ from . import splitkv as _k
 
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
-                 device="cuda", kernel=_k.KERNEL_AUTO):
+                 device="cuda", kernel=_k.KERNEL_AUTO, fused=False):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -30,6 +30,8 @@ class SplitKVAttention:
         self.dtype = dtype
         self.device = torch.device(device)
         self.kernel = kernel
+        self.fused = bool(fused)
+        self._tickets = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
         self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
@@ -101,11 +103,26 @@ class SplitKVAttention:
         _k.splitkv_merge(self._o_part, self._lse_part, self._work_dev, self.B, self.total_q, out, lse,
                          stream=stream)
 
+    def fused_call(self, q, k_pool, v_pool, block_table, scale, out, lse, stream=None):
+        if self._tickets is None:
+            n = _k.splitkv_ticket_count(self.B, self.Hq, self.Hkv, self.max_q_len)
+            self._tickets = torch.zeros(n, dtype=torch.int32, device=self.device)
+        _k.splitkv_attn_fused(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+                              self.total_q, self.max_q_len, self.block_len, scale, self.causal, self._o_part,
+                              self._lse_part, self._tickets, out, lse, kernel=self.kernel, stream=stream)
+
+    @property
+    def tickets(self):
+        return self._tickets
+
     def __call__(self, q, k_pool, v_pool, block_table, scale, out=None, lse=None, stream=None):
         if out is None:
             out = torch.empty((self.total_q, self.Hq, self.d), dtype=q.dtype, device=q.device)
         if lse is None:
             lse = torch.empty((self.total_q, self.Hq), dtype=torch.float32, device=q.device)
-        self.partial(q, k_pool, v_pool, block_table, scale, stream=stream)
-        self.merge(out, lse, stream=stream)
+        if self.fused:
+            self.fused_call(q, k_pool, v_pool, block_table, scale, out, lse, stream=stream)
+        else:
+            self.partial(q, k_pool, v_pool, block_table, scale, stream=stream)
+            self.merge(out, lse, stream=stream)
         return out, lse

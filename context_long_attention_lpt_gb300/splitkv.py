@@ -34,6 +34,10 @@ _SIGNATURES = {
                                              _i32, _i32, _i32, _i32, _f32, _i32, _i32, _p, _p, _i64,
                                              _i32, _p]),
     "splitkv_merge": (ctypes.c_int, [_p, _p, _i64, _p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]),
+    "splitkv_ticket_count": (_i64, [_i32, _i32, _i32, _i32]),
+    "splitkv_attn_fused": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+                                          _i32, _i32, _f32, _i32, _i32, _p, _p, _i64, _p, _i64, _p, _p, _i32,
+                                          _p]),
     "splitkv_attention_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i64, _i32, _i32, _i32,
                                                   _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i64, _p,
                                                   _p, _p]),
@@ -176,6 +180,31 @@ def splitkv_attn_partial(q, k_pool, v_pool, block_table, work, n_items, B, total
         block_table.shape[1], work.data_ptr(), n_items, B, total_q, max_q_len, hq, hkv, d, block_len,
         float(scale), int(bool(causal)), _dtype_code(q), o_part.data_ptr(), lse_part.data_ptr(),
         o_part.shape[0], kernel, _stream_handle(stream)))
+
+
+def splitkv_ticket_count(B, Hq, Hkv, max_q_len):
+    return _check("splitkv_ticket_count", lib().splitkv_ticket_count(B, Hq, Hkv, max_q_len))
+
+
+def splitkv_attn_fused(q, k_pool, v_pool, block_table, work, n_items, B, total_q, max_q_len, block_len, scale,
+                       causal, o_part, lse_part, tickets, out, lse_out, kernel=KERNEL_AUTO, stream=None):
+    """Partial attention + merge (one launch with the decode kernel); tickets: zeroed int32/uint32 device
+    tensor of at least splitkv_ticket_count(...) elements, left zeroed."""
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
+                    ("work", work), ("o_part", o_part), ("lse_part", lse_part), ("tickets", tickets),
+                    ("out", out), ("lse_out", lse_out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _, hq, d = q.shape
+    n_pool, bl, hkv, d2 = k_pool.shape
+    if d2 != d or bl != block_len:
+        raise ValueError("k_pool shape does not match q / block_len")
+    _check("splitkv_attn_fused", lib().splitkv_attn_fused(
+        q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), n_pool, block_table.data_ptr(),
+        block_table.shape[1], work.data_ptr(), n_items, B, total_q, max_q_len, hq, hkv, d, block_len,
+        float(scale), int(bool(causal)), _dtype_code(q), o_part.data_ptr(), lse_part.data_ptr(),
+        o_part.shape[0], tickets.data_ptr(), tickets.numel(), out.data_ptr(), lse_out.data_ptr(), kernel,
+        _stream_handle(stream)))
 
 
 def splitkv_merge(o_part, lse_part, work, B, total_q, out, lse_out, stream=None):

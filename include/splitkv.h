@@ -135,6 +135,30 @@ int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
                          int32_t causal, int32_t dtype, float* o_part, float* lse_part,
                          int64_t part_rows, int32_t kernel, void* stream);
 
+/* Counters splitkv_attn_fused needs: B * Hkv * max(1, ceil(max_q_len*(Hq/Hkv)/256)). */
+int64_t splitkv_ticket_count(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len);
+
+/* Steps 3 and 4 in one call (Split-KV card, "All Facts": exact, "Timeline":
+ * query-sized partials): the partial attention of splitkv_attn_partial and the
+ * merge of splitkv_merge, with the same arguments and results.  With the decode
+ * kernel both happen in ONE launch: each CTA writes its partial rows, publishes
+ * them (memory fence) and takes a ticket from the counter of its (sequence, K/V
+ * head) group with an atomic add; the CTA that takes the last ticket merges the
+ * group's partials into out / lse_out and sets the counter back to zero.  No CTA
+ * waits for another.  Other kernels run the partial and merge launches in turn.
+ *   tickets (device, caller-owned): n_tickets >= splitkv_ticket_count(...)
+ *   uint32 counters, all zero before the first call; every completed call leaves
+ *   them zero again.  After a call that reported a device error (status word),
+ *   zero them before the next call.  Calls that overlap on the GPU must use
+ *   different ticket buffers (and partial buffers). */
+int splitkv_attn_fused(const void* q, const void* k_pool, const void* v_pool,
+                       int64_t n_pool_blocks, const int32_t* block_table,
+                       int32_t max_blocks_per_seq, const int32_t* work, int32_t n_items,
+                       int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq, int32_t Hkv,
+                       int32_t d, int32_t block_len, float scale, int32_t causal, int32_t dtype,
+                       float* o_part, float* lse_part, int64_t part_rows, uint32_t* tickets,
+                       int64_t n_tickets, void* out, float* lse_out, int32_t kernel, void* stream);
+
 /* Step 4, exact merge of the partials (Split-KV card, "All Facts": identical to
  * the unsharded result).  For every query row r of sequence b and head h, over
  * the items i of b:  L = ln sum_i exp(L_i),  O = sum_i exp(L_i - L) O_i;

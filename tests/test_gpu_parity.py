@@ -165,3 +165,43 @@ def test_bad_arguments_raise_before_launch():
     with pytest.raises(K.SplitKVError):  # tensor-core kernel does not take block_len % 128 != 0
         w2 = wl.custom("shortq", q_len=40, context=1000, block_len=200, n_shards=2)
         run_cuda(w2, kernel=K.KERNEL_TC)
+
+
+@pytest.mark.parametrize("name", ["decode_small", "decode_gqa8", "shortq_small", "tiny"])
+def test_fused_single_launch_matches_oracle(name):
+    """splitkv_attn_fused: the decode kernel merges in its own launch (last CTA per group);
+    other kernels fall back to two launches.  Two calls in a row: the tickets return to zero."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=True)
+    o_ref, l_ref = full_reference(inp)
+    for _ in range(2):
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        torch.cuda.synchronize()
+        eo, el = max_errors(out, lse, o_ref, l_ref)
+        assert_close(w, eo, el, f"fused {name}")
+        assert int(run.tickets.abs().sum()) == 0
+    assert K.splitkv_device_status() == 0
+
+
+def test_fused_decode_full_size_and_ragged():
+    w = wl.WORKLOADS["decode"]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=True)
+    out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    torch.cuda.synchronize()
+    eo, el = compare_rows(inp, out, lse, sample_rows(inp, 64, seed=3))
+    assert_close(w, eo, el, "fused decode full size")
+    # ragged batch with an empty sequence and a single-key sequence
+    w2 = wl.custom("decode", B=4, n_shards=5)
+    lens = ([1, 0, 1, 1], [1, 0, 777, 300])
+    inp2 = wl.make_inputs(w2, device="cuda", poison_tail=True, lens=lens)
+    run2 = SplitKVAttention(inp2.q_len, inp2.kv_len, w2.block_len, w2.causal, w2.n_shards, w2.Hq, w2.Hkv,
+                            w2.d, inp2.q.dtype, fused=True)
+    out2, lse2 = run2(inp2.q, inp2.k_pool, inp2.v_pool, inp2.block_table, w2.scale)
+    torch.cuda.synchronize()
+    eo, el = max_errors(out2, lse2, *full_reference(inp2))
+    assert_close(w2, eo, el, "fused ragged")
+    assert int(run2.tickets.abs().sum()) == 0
