@@ -47,6 +47,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--fused", action="store_true",
                     help="splitkv_attn_fused (one launch with the decode kernel) instead of partial + merge")
+    ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
+                    help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
+                         "reduction completion model (splitkv_plan_dcp)")
     ap.add_argument("--context", type=int, default=None,
                     help="override the context length (smaller cases for profiling)")
     return ap.parse_args(argv)
@@ -198,6 +201,14 @@ def traffic_for(kernel_name, workload):
     return float(e["bytes_per_launch"])
 
 
+def dcp_model(w):
+    """Costs of the split-selection model for a context-parallel deployment of this
+    workload: alpha = seconds per unit of block cost on one rank (4*d*Hq flops at
+    1200 TFLOP/s, the tensor-core kernel's measured rate), beta = seconds per partial
+    row exchanged and merged (Hq*(d+1)*4 bytes at 900 GB/s of NVLink)."""
+    return 4.0 * w.d * w.Hq / 1.2e15, w.Hq * (w.d + 1) * 4.0 / 0.9e12
+
+
 # -------------------------------------------------------------- our arm
 
 
@@ -218,8 +229,10 @@ def run_ours(args, dctx):
     kernel = {"auto": K.KERNEL_AUTO, "simt": K.KERNEL_SIMT, "decode": K.KERNEL_DECODE,
               "tc": K.KERNEL_TC}[args.kernel]
     inp = wl.make_inputs(w, device=f"cuda:{dev}")
+    alpha, beta = dcp_model(w)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
-                           inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused)
+                           inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
+                           planner=args.planner, dcp_alpha=alpha, dcp_beta=beta)
     fused_one_launch = run.fused and run.kernel_used() == K.KERNEL_DECODE
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
@@ -308,7 +321,8 @@ def run_ours(args, dctx):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "tflops": acc["flops"] * args.steps * dctx.world / t_max / 1e12,
         "config": {"workload": w.name, "shape": w.description, "kernel": kname,
-                   "n_items": run.n_items, "lpt_imbalance": run.imbalance,
+                   "n_items": run.n_items, "lpt_imbalance": run.imbalance, "planner": args.planner,
+                   "shards_used": run.n_shards_used, "part_rows": run.part_rows,
                    "planner_us": planner_us, "host_s": host_s,
                    "l2": f"inputs larger than L2 (K/V {acc['kv_bytes'] / 1e9:.2f} GB vs L2 "
                          f"{L2_BYTES / 1e6:.0f} MB); no flush"

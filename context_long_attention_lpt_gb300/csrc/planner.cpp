@@ -277,3 +277,66 @@ extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, i
   splitkv::clear_error();
   return SPLITKV_OK;
 }
+
+extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
+                                int32_t causal, int32_t max_shards, double alpha, double beta,
+                                int32_t* shard_of_block, int64_t n_blocks, int64_t* shard_load,
+                                int32_t* n_shards_used, double* modeled_time) {
+  // Split selection that models attention completion together with the reduction
+  // that depends on it (LiquidCP abstract: MegaDCP).  For every shard count s the
+  // blocks are planned with the same LPT rule; the shards run concurrently, so
+  // attention completes with the most loaded one, and the reduction combines one
+  // partial row per (shard, sequence) pair and query token:
+  //     T(s) = alpha * max_load(s) + beta * partial_rows(s)
+  // The smallest s reaching the least T wins.
+  int st = 0;
+  if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
+  if (max_shards <= 0 || !shard_of_block || !shard_load || !n_shards_used || !modeled_time)
+    return fail(SPLITKV_ERR_INVALID, "splitkv_plan_dcp: bad arguments");
+  std::vector<int64_t> costs(static_cast<size_t>(n_blocks));
+  st = splitkv_block_costs(q_len, kv_len, B, block_len, causal, costs.data(), n_blocks);
+  if (st != SPLITKV_OK) return st;
+  std::vector<int32_t> seq_of(static_cast<size_t>(n_blocks));
+  {
+    int64_t g = 0;
+    for (int32_t b = 0; b < B; ++b)
+      for (int64_t j = 0; j < (static_cast<int64_t>(kv_len[b]) + block_len - 1) / block_len; ++j) seq_of[g++] = b;
+  }
+  std::vector<int32_t> sob(static_cast<size_t>(n_blocks)), best_sob;
+  std::vector<int64_t> load(static_cast<size_t>(max_shards)), best_load;
+  std::vector<uint8_t> held(static_cast<size_t>(max_shards));
+  int32_t best_s = 0;
+  double best_t = 0.0;
+  for (int32_t s = 1; s <= max_shards; ++s) {
+    st = splitkv_plan(costs.data(), n_blocks, s, sob.data(), load.data());
+    if (st != SPLITKV_OK) return st;
+    int64_t max_load = 0;
+    for (int32_t k = 0; k < s; ++k) max_load = std::max(max_load, load[k]);
+    // partial rows: blocks are sequence-major, so one pass with a per-sequence shard mask
+    int64_t rows = 0;
+    for (int64_t g = 0; g < n_blocks;) {
+      const int32_t b = seq_of[g];
+      std::fill(held.begin(), held.begin() + s, 0);
+      int32_t distinct = 0;
+      for (; g < n_blocks && seq_of[g] == b; ++g)
+        if (!held[sob[g]]) {
+          held[sob[g]] = 1;
+          ++distinct;
+        }
+      rows += static_cast<int64_t>(distinct) * q_len[b];
+    }
+    const double t = alpha * static_cast<double>(max_load) + beta * static_cast<double>(rows);
+    if (best_s == 0 || t < best_t) {
+      best_s = s;
+      best_t = t;
+      best_sob = sob;
+      best_load.assign(load.begin(), load.begin() + s);
+    }
+  }
+  std::copy(best_sob.begin(), best_sob.end(), shard_of_block);
+  for (int32_t k = 0; k < max_shards; ++k) shard_load[k] = k < best_s ? best_load[k] : 0;
+  *n_shards_used = best_s;
+  *modeled_time = best_t;
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}

@@ -19,7 +19,8 @@ from . import splitkv as _k
 
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
-                 device="cuda", kernel=_k.KERNEL_AUTO, fused=False):
+                 device="cuda", kernel=_k.KERNEL_AUTO, fused=False, planner="lpt", dcp_alpha=1.0,
+                 dcp_beta=0.0):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -31,6 +32,11 @@ class SplitKVAttention:
         self.device = torch.device(device)
         self.kernel = kernel
         self.fused = bool(fused)
+        if planner not in ("lpt", "dcp"):
+            raise ValueError("planner must be 'lpt' or 'dcp'")
+        self.planner = planner
+        self.dcp_alpha, self.dcp_beta = float(dcp_alpha), float(dcp_beta)
+        self.n_shards_used = self.n_shards
         self._tickets = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
@@ -48,7 +54,12 @@ class SplitKVAttention:
         """Block costs, LPT plan and work lists on the host; copy the work to the device."""
         self.block_cost = _k.splitkv_block_costs(self._q_len_np, self._kv_len_np, self.block_len,
                                                  self.causal)
-        self.shard_of_block, self.shard_load = _k.splitkv_plan(self.block_cost, self.n_shards)
+        if self.planner == "lpt":
+            self.shard_of_block, self.shard_load = _k.splitkv_plan(self.block_cost, self.n_shards)
+        else:
+            self.n_shards_used, self.shard_of_block, self.shard_load, self.modeled_time = _k.splitkv_plan_dcp(
+                self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
+                self.dcp_beta)
         work, self.n_items, self.part_rows = _k.splitkv_build_work(
             self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
             self.n_shards)
@@ -71,7 +82,7 @@ class SplitKVAttention:
 
     @property
     def imbalance(self):
-        load = self.shard_load
+        load = self.shard_load[: self.n_shards_used]
         mean = load.sum() / len(load)
         return float(load.max() / mean - 1.0) if mean > 0 else 0.0
 

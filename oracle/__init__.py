@@ -22,6 +22,9 @@ knowledge card, kongchang.com):
   longest-processing-time-first allocation of context KV blocks to shards and
   its load-imbalance rate ("Timeline" / "All Facts": cost-aware LPT, load
   imbalance below 1%).
+* ``dcp_select`` - split selection that models attention completion together
+  with the dependent reduction (LiquidCP abstract, PaperTrail: MegaDCP), built
+  on the same LPT plans.
 
 Everything is written for readability, not speed: fp64 throughout, a library
 matmul / sort as the only primitives, no blocking or fusion beyond what the
@@ -29,7 +32,7 @@ definitions state.
 """
 
 from .attn import attention, attention_rows, partial, merge, visible_keys, gather_sequence
-from .lpt import block_costs, lpt_assign, imbalance, shard_key_sets
+from .lpt import block_costs, lpt_assign, imbalance, shard_key_sets, partial_rows, dcp_select
 
 __all__ = [
     "attention",
@@ -42,4 +45,6 @@ __all__ = [
     "lpt_assign",
     "imbalance",
     "shard_key_sets",
+    "partial_rows",
+    "dcp_select",
 ]

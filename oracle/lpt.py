@@ -81,3 +81,38 @@ def shard_key_sets(shard_of_block, kv_len, block_len, n_shards):
             sets[shard_of_block[g]][b].append(j)
             g += 1
     return sets
+
+
+def partial_rows(shard_of_block, q_len, kv_len, block_len):
+    """Rows the merge has to reduce: sum over distinct (shard, sequence) pairs of q_len."""
+    pairs = set()
+    g = 0
+    for b, lk in enumerate(kv_len):
+        for _ in range(-(-int(lk) // block_len)):
+            pairs.add((shard_of_block[g], b))
+            g += 1
+    return sum(int(q_len[b]) for _, b in pairs)
+
+
+def dcp_select(q_len, kv_len, block_len, causal, max_shards, alpha, beta):
+    """Split selection that models attention completion together with its reduction.
+
+    After the LiquidCP abstract (PaperTrail, arXiv 2611.04401): MegaDCP picks
+    history-KV splits by jointly modelling the completion of attention and of the
+    reductions that depend on it.  The abstract gives no formula; the reading
+    taken here: for every shard count s in 1..max_shards, plan the blocks with
+    the cost-aware LPT rule onto s shards; the shards run concurrently, so
+    attention completes with the most loaded shard, and the reduction then has
+    to combine one partial row per (shard, sequence) pair and query token:
+        T(s) = alpha * max_load(s) + beta * partial_rows(s)
+    (evaluated in IEEE double exactly in this order).  The smallest s reaching
+    the least T wins.  Returns (s, shard_of_block, load, T(s)).
+    """
+    costs = block_costs(q_len, kv_len, block_len, causal)
+    best = None
+    for s in range(1, max_shards + 1):
+        sob, load = lpt_assign(costs, s)
+        t = float(alpha) * float(max(load)) + float(beta) * float(partial_rows(sob, q_len, kv_len, block_len))
+        if best is None or t < best[3]:
+            best = (s, sob, load, t)
+    return best

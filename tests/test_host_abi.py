@@ -182,3 +182,41 @@ def test_work_buffer_too_small_is_capacity_error(k):
     st = L.splitkv_build_work(p(q), p(kv), 1, 4, p(c), p(sob), len(c), 2, p(work), 4,
                               ctypes.byref(n_items), ctypes.byref(rows))
     assert st == -4
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.0, 1e9), (1.0, 100.0), (0.25, 3.5)])
+def test_dcp_selection_matches_oracle(k, name, alpha, beta):
+    w = wl.WORKLOADS[name]
+    q, kv = wl.lengths(w)
+    s, sob, load, t = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta)
+    rs, rsob, rload, rt = oracle.dcp_select(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta)
+    assert (s, sob.tolist(), load[:s].tolist(), t) == (rs, rsob, rload, rt)
+    assert (load[s:] == 0).all()
+
+
+def test_fuzz_dcp_selection(k):
+    rng = random.Random(77)
+    for case in range(300):
+        B = rng.randint(1, 4)
+        q = [rng.randint(1, 30) for _ in range(B)]
+        kv = [qq + rng.randint(0, 200) for qq in q]
+        bl = rng.choice([4, 16, 32])
+        S = rng.randint(1, 8)
+        a, b = rng.choice([0.0, 1.0, 2.5]), rng.choice([0.0, 0.5, 7.0, 1e6])
+        causal = rng.random() < 0.5
+        got = k.splitkv_plan_dcp(q, kv, bl, causal, S, a, b)
+        ref = oracle.dcp_select(q, kv, bl, causal, S, a, b)
+        assert (got[0], got[1].tolist(), got[3]) == (ref[0], ref[1], ref[3]), case
+
+
+def test_dcp_extremes(k):
+    """No reduction cost: the least makespan wins; prohibitive reduction cost: one shard."""
+    w = wl.WORKLOADS["varlen"]
+    q, kv = wl.lengths(w)
+    costs = oracle.block_costs(q, kv, w.block_len, w.causal)
+    s, _, load, t = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, 1.0, 0.0)
+    best = min(max(oracle.lpt_assign(costs, m)[1]) for m in range(1, w.n_shards + 1))
+    assert t == best and max(load) == best
+    s1, sob1, _, _ = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, 1.0, 1e12)
+    assert s1 == 1 and set(sob1.tolist()) == {0}
