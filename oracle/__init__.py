@@ -22,6 +22,10 @@ knowledge card, kongchang.com):
   longest-processing-time-first allocation of context KV blocks to shards and
   its load-imbalance rate ("Timeline" / "All Facts": cost-aware LPT, load
   imbalance below 1%).
+* ``attention_backward`` / ``partial_backward`` / ``delta`` - fp64 gradients
+  dQ, dK, dV of the same attention, unsharded and restricted to one shard's
+  keys (card intro: a training method; "All Facts": exact), from the merged
+  forward's L and D = rowsum(dO * O).
 * ``dcp_select`` - split selection that models attention completion together
   with the dependent reduction (LiquidCP abstract, PaperTrail: MegaDCP), built
   on the same LPT plans.
@@ -32,9 +36,13 @@ definitions state.
 """
 
 from .attn import attention, attention_rows, partial, merge, visible_keys, gather_sequence
+from .backward import attention_backward, partial_backward, delta
 from .lpt import block_costs, lpt_assign, imbalance, shard_key_sets, partial_rows, dcp_select
 
 __all__ = [
+    "attention_backward",
+    "partial_backward",
+    "delta",
     "attention",
     "attention_rows",
     "partial",
