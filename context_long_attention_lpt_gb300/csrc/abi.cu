@@ -222,3 +222,53 @@ extern "C" int splitkv_device_status(uint32_t* status, int32_t clear) {
   splitkv::clear_error();
   return SPLITKV_OK;
 }
+
+extern "C" int splitkv_bwd_delta(const void* o, const void* dout, int32_t total_q, int32_t Hq, int32_t d,
+                                 int32_t dtype, float* delta, void* stream) {
+  if (dtype != SPLITKV_F32 && dtype != SPLITKV_BF16) return fail(SPLITKV_ERR_INVALID, "bad dtype");
+  if (total_q < 0 || Hq <= 0 || (d != 64 && d != 128)) return fail(SPLITKV_ERR_INVALID, "bad sizes");
+  if (total_q > 0 && (!o || !dout || !delta)) return fail(SPLITKV_ERR_INVALID, "null device pointer");
+  const cudaError_t e = splitkv::launch_bwd_delta(o, dout, static_cast<int64_t>(total_q) * Hq, d, dtype, delta,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "delta launch: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int splitkv_attn_backward(const void* q, const void* k_pool, const void* v_pool, int64_t n_pool_blocks,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* work,
+                                     int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,
+                                     int32_t Hkv, int32_t d, int32_t block_len, float scale, int32_t causal,
+                                     int32_t dtype, const void* dout, const float* lse, const float* delta,
+                                     float* dq_part, int64_t part_rows, float* dk_pool, float* dv_pool,
+                                     void* stream) {
+  splitkv::PartialArgs a;
+  int st = make_partial_args(&a, q, k_pool, v_pool, n_pool_blocks, block_table, max_blocks_per_seq, work, n_items, B,
+                             total_q, max_q_len, Hq, Hkv, d, block_len, scale, causal, dtype, dq_part,
+                             /* lse_part: unused */ dq_part, part_rows, SPLITKV_KERNEL_SIMT);
+  if (st != SPLITKV_OK) return st;
+  if (n_items > 0 && (!dout || !lse || !delta || !dk_pool || !dv_pool))
+    return fail(SPLITKV_ERR_INVALID, "null device pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the partial dQ rows collect atomic adds from every key tile of their item
+  cudaError_t e = cudaMemsetAsync(dq_part, 0, static_cast<size_t>(part_rows) * Hq * d * sizeof(float), s);
+  if (e == cudaSuccess && n_items > 0) e = splitkv::launch_bwd_partial(a, dout, lse, delta, dq_part, dk_pool, dv_pool, s);
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
+extern "C" int splitkv_dq_reduce(const float* dq_part, int64_t part_rows, const int32_t* work, int32_t B,
+                                 int32_t total_q, int32_t Hq, int32_t d, float* dq, void* stream) {
+  if (B <= 0 || Hq <= 0 || total_q < 0 || part_rows < 0 || (d != 64 && d != 128))
+    return fail(SPLITKV_ERR_INVALID, "bad sizes");
+  if (total_q > 0 && (!dq_part || !work || !dq)) return fail(SPLITKV_ERR_INVALID, "null device pointer");
+  int err = 0;
+  unsigned int* status = status_word(&err);
+  if (!status) return err;
+  const cudaError_t e = splitkv::launch_dq_reduce(dq_part, part_rows, work, B, total_q, Hq, d, dq, status,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "dq reduce launch: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}

@@ -52,6 +52,14 @@ bool decode_supports(const PartialArgs& a);
 bool decode_fuses(const PartialArgs& a);  // the decode kernel can merge in the same launch
 bool tc_supports(const PartialArgs& a);
 
+// Backward pass (backward.cu).
+cudaError_t launch_bwd_delta(const void* o, const void* dout, int64_t n_rows, int32_t d, int32_t dtype, float* delta,
+                             cudaStream_t stream);
+cudaError_t launch_bwd_partial(const PartialArgs& a, const void* dout, const float* lse, const float* delta,
+                               float* dq_part, float* dk_pool, float* dv_pool, cudaStream_t stream);
+cudaError_t launch_dq_reduce(const float* dq_part, int64_t part_rows, const int32_t* work, int32_t B, int32_t total_q,
+                             int32_t Hq, int32_t d, float* dq, unsigned int* status, cudaStream_t stream);
+
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int64_t part_rows,
                          const int32_t* work, int32_t B, int32_t total_q, int32_t Hq, int32_t d,
                          int32_t dtype, void* out, float* lse_out, unsigned int* status,

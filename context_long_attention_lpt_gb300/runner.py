@@ -114,6 +114,22 @@ class SplitKVAttention:
         _k.splitkv_merge(self._o_part, self._lse_part, self._work_dev, self.B, self.total_q, out, lse,
                          stream=stream)
 
+    def backward(self, q, k_pool, v_pool, block_table, scale, out, lse, dout, stream=None):
+        """Gradients of the forward pass that produced (out, lse) for upstream gradient dout.
+        Returns (dq fp32 [total_q, Hq, d], dk_pool, dv_pool fp32 like the pools; zero where no key)."""
+        dev = q.device
+        delta = torch.empty((self.total_q, self.Hq), dtype=torch.float32, device=dev)
+        _k.splitkv_bwd_delta(out, dout, delta, stream=stream)
+        dq_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32, device=dev)
+        dk = torch.zeros(tuple(k_pool.shape), dtype=torch.float32, device=dev)
+        dv = torch.zeros(tuple(v_pool.shape), dtype=torch.float32, device=dev)
+        _k.splitkv_attn_backward(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+                                 self.total_q, self.max_q_len, self.block_len, scale, self.causal, dout, lse,
+                                 delta, dq_part, dk, dv, stream=stream)
+        dq = torch.empty((self.total_q, self.Hq, self.d), dtype=torch.float32, device=dev)
+        _k.splitkv_dq_reduce(dq_part, self._work_dev, self.B, self.total_q, dq, stream=stream)
+        return dq, dk, dv
+
     def fused_call(self, q, k_pool, v_pool, block_table, scale, out, lse, stream=None):
         if self._tickets is None:
             n = _k.splitkv_ticket_count(self.B, self.Hq, self.Hkv, self.max_q_len)

@@ -43,6 +43,10 @@ _SIGNATURES = {
     "splitkv_attention_noalloc": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i64, _i32, _i32, _i32,
                                                   _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i64, _p,
                                                   _p, _p]),
+    "splitkv_bwd_delta": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, _p, _p]),
+    "splitkv_attn_backward": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+                                             _i32, _i32, _f32, _i32, _i32, _p, _p, _p, _p, _i64, _p, _p, _p]),
+    "splitkv_dq_reduce": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, _i32, _i32, _p, _p]),
     "splitkv_device_status": (ctypes.c_int, [_p, _i32]),
     "splitkv_last_error": (ctypes.c_char_p, []),
 }
@@ -250,6 +254,33 @@ def splitkv_attention_noalloc(q, k_pool, v_pool, block_table, work_host, n_items
         block_table.shape[1], _ptr(work), work.size, n_items, B, total_q, max_q_len, hq, hkv, d, block_len,
         float(scale), int(bool(causal)), _dtype_code(q), part_rows, out.data_ptr(), lse_out.data_ptr(),
         _stream_handle(stream)))
+
+
+def splitkv_bwd_delta(o, dout, delta, stream=None):
+    total_q, hq, d = o.shape
+    _check("splitkv_bwd_delta", lib().splitkv_bwd_delta(o.data_ptr(), dout.data_ptr(), total_q, hq, d,
+                                                       _dtype_code(o), delta.data_ptr(), _stream_handle(stream)))
+
+
+def splitkv_attn_backward(q, k_pool, v_pool, block_table, work, n_items, B, total_q, max_q_len, block_len, scale,
+                          causal, dout, lse, delta, dq_part, dk_pool, dv_pool, stream=None):
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("dout", dout), ("lse", lse),
+                    ("delta", delta), ("dq_part", dq_part), ("dk_pool", dk_pool), ("dv_pool", dv_pool)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _, hq, d = q.shape
+    n_pool, bl, hkv, _ = k_pool.shape
+    _check("splitkv_attn_backward", lib().splitkv_attn_backward(
+        q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), n_pool, block_table.data_ptr(), block_table.shape[1],
+        work.data_ptr(), n_items, B, total_q, max_q_len, hq, hkv, d, block_len, float(scale), int(bool(causal)),
+        _dtype_code(q), dout.data_ptr(), lse.data_ptr(), delta.data_ptr(), dq_part.data_ptr(), dq_part.shape[0],
+        dk_pool.data_ptr(), dv_pool.data_ptr(), _stream_handle(stream)))
+
+
+def splitkv_dq_reduce(dq_part, work, B, total_q, dq, stream=None):
+    _, hq, d = dq.shape
+    _check("splitkv_dq_reduce", lib().splitkv_dq_reduce(dq_part.data_ptr(), dq_part.shape[0], work.data_ptr(), B,
+                                                       total_q, hq, d, dq.data_ptr(), _stream_handle(stream)))
 
 
 def splitkv_device_status(clear=False):

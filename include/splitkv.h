@@ -223,6 +223,44 @@ int splitkv_attention_noalloc(const void* q, const void* k_pool, const void* v_p
                               int32_t block_len, float scale, int32_t causal, int32_t dtype,
                               int64_t part_rows, void* out, float* lse_out, void* stream);
 
+/* ------------------------------------------------------------ backward pass
+ * The Split-KV card presents the method for training (intro: asymmetric
+ * training with very short queries and very long contexts) and as exact ("All
+ * Facts").  With the merged forward's O and L, each shard needs only
+ * query-sized tensors (Q, dO, L, D) to compute the exact dK, dV of its own keys
+ * and a query-sized partial dQ; the partials sum to dQ.  Chain rule through
+ * s = scale q.k, P = exp(s - L), O = P V, for every visible (row r, key j):
+ *   dV_j += P_rj dO_r, dP_rj = dO_r.V_j, dS_rj = P_rj (dP_rj - D_r),
+ *   dQ_r += scale dS_rj K_j, dK_j += scale dS_rj Q_r.                        */
+
+/* D[row, h] = sum_c O[row, h, c] * dO[row, h, c].  In (device, dtype): o, dout
+ * [total_q, Hq, d] (O = splitkv_merge's output).  Out (device): delta fp32
+ * [total_q, Hq]. */
+int splitkv_bwd_delta(const void* o, const void* dout, int32_t total_q, int32_t Hq, int32_t d,
+                      int32_t dtype, float* delta, void* stream);
+
+/* Per-shard backward over the work items of splitkv_build_work (CUDA cores).
+ * In (device): q, k_pool, v_pool, block_table, work as for the forward; dout
+ * [total_q, Hq, d] (dtype); lse fp32 [total_q, Hq] (splitkv_merge's lse_out);
+ * delta fp32 [total_q, Hq].  Out (device, fp32): dq_part [part_rows, Hq, d]
+ * (item i's partial dQ in its part_row slab; zeroed and accumulated by this
+ * call), dk_pool / dv_pool [n_pool_blocks, block_len, Hkv, d]: the gradient of
+ * every key position < kv_len of every sequence is written; other positions
+ * are left untouched. */
+int splitkv_attn_backward(const void* q, const void* k_pool, const void* v_pool, int64_t n_pool_blocks,
+                          const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* work,
+                          int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,
+                          int32_t Hkv, int32_t d, int32_t block_len, float scale, int32_t causal,
+                          int32_t dtype, const void* dout, const float* lse, const float* delta,
+                          float* dq_part, int64_t part_rows, float* dk_pool, float* dv_pool,
+                          void* stream);
+
+/* dQ[row, h] = sum over the items of the row's sequence of their partial dQ
+ * rows (the backward's query-sized exchange).  Out (device): dq fp32
+ * [total_q, Hq, d]. */
+int splitkv_dq_reduce(const float* dq_part, int64_t part_rows, const int32_t* work, int32_t B,
+                      int32_t total_q, int32_t Hq, int32_t d, float* dq, void* stream);
+
 /* Reads and optionally clears the device status word: bit 0, a logical block
  * past max_blocks_per_seq or a block-table entry outside the pool was skipped;
  * bit 1, a work item's partial rows fell outside part_rows (item skipped).
