@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
                     help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
                          "reduction completion model (splitkv_plan_dcp)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (delta, per-shard dK/dV + partial dQ, dQ reduce) instead")
     ap.add_argument("--context", type=int, default=None,
                     help="override the context length (smaller cases for profiling)")
     return ap.parse_args(argv)
@@ -256,6 +258,8 @@ def run_ours(args, dctx):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.backward:
+        return run_backward(args, dctx, w, inp, run, out, lse, acc)
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
@@ -335,6 +339,37 @@ def run_ours(args, dctx):
     }
     if dctx.rank == 0 and dctx.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if dctx.rank == 0:
+        print(json.dumps(line), flush=True)
+    dctx.finish()
+
+
+def run_backward(args, dctx, w, inp, run, out, lse, acc):
+    """Backward pass of the same plan: the forward output is computed once (untimed), then
+    K timed backward steps.  Algorithmic flops = 2.5 x forward (QK^T recompute, dP, dV, dQ, dK)."""
+    import torch
+
+    g = torch.Generator(device=out.device).manual_seed(0)
+    dout = torch.randn(out.shape, generator=g, device=out.device, dtype=torch.float32).to(out.dtype)
+    for _ in range(2):
+        run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+    t1.record()
+    torch.cuda.synchronize()
+    s = t0.elapsed_time(t1) / 1e3 / args.steps
+    flops = 2.5 * acc["flops"]
+    peaks, src = load_peaks()
+    line = {"metric": METRIC + " (backward pass)", "value": flops / s / 1e12, "unit": "TFLOP/s",
+            "n_gpus": dctx.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s,
+            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.description, "kernel": "backward_simt"},
+            "roofline": {"bound": "fp32_fma", "achieved": flops / s / 1e12, "unit": "TFLOP/s",
+                         "note": "CUDA-core kernel: bf16 inputs, fp32 FMA arithmetic"}}
     if dctx.rank == 0:
         print(json.dumps(line), flush=True)
     dctx.finish()

@@ -36,13 +36,15 @@ definitions state.
 """
 
 from .attn import attention, attention_rows, partial, merge, visible_keys, gather_sequence
-from .backward import attention_backward, partial_backward, delta
+from .backward import attention_backward, partial_backward, delta, backward_rows, backward_keys
 from .lpt import block_costs, lpt_assign, imbalance, shard_key_sets, partial_rows, dcp_select
 
 __all__ = [
     "attention_backward",
     "partial_backward",
     "delta",
+    "backward_rows",
+    "backward_keys",
     "attention",
     "attention_rows",
     "partial",

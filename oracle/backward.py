@@ -92,3 +92,81 @@ def attention_backward(q, k_pool, v_pool, block_table, q_len, kv_len, block_len,
     all_blocks = [list(range(-(-int(n) // int(block_len)))) for n in kv_len]
     return partial_backward(q, k_pool, v_pool, block_table, q_len, kv_len, block_len, causal, scale, do, lse, dlt,
                             all_blocks)
+
+
+def _seq_head(pool, table_row, lk, block_len, kvh):
+    return gather_sequence(pool[:, :, kvh], table_row, lk, block_len)
+
+
+def backward_rows(q, k_pool, v_pool, block_table, q_len, kv_len, block_len, causal, scale, do, rows):
+    """dQ of selected rows (b, t, h), each from its own full forward over the visible keys.
+
+    Returns dQ [n, d] in fp64.  Every step follows ``partial_backward`` for one row.
+    """
+    hq = q.shape[1]
+    g = hq // k_pool.shape[2]
+    cu = _offsets(q_len)
+    out = torch.zeros((len(rows), q.shape[2]), dtype=torch.float64)
+    cache = {}
+    for i, (b, t, h) in enumerate(rows):
+        lq, lk = int(q_len[b]), int(kv_len[b])
+        key = (b, h // g)
+        if key not in cache:
+            cache.clear()
+            cache[key] = (_seq_head(k_pool, block_table[b], lk, block_len, h // g),
+                          _seq_head(v_pool, block_table[b], lk, block_len, h // g))
+        kh, vh = cache[key]
+        n_vis = visible_keys(lq, lk, t, causal)
+        qr = q[cu[b] + t, h].to(torch.float64)
+        dor = do[cu[b] + t, h].to(torch.float64)
+        s = scale * (kh[:n_vis] @ qr)
+        p = torch.softmax(s, dim=0)
+        o = p @ vh[:n_vis]
+        dp = vh[:n_vis] @ dor
+        ds = p * (dp - torch.dot(dor, o))
+        out[i] = scale * (ds @ kh[:n_vis])
+    return out
+
+
+def backward_keys(q, k_pool, v_pool, block_table, q_len, kv_len, block_len, causal, scale, do, keys, row_chunk=64):
+    """dK, dV of selected keys (b, kvh, position): every query row of the K/V head's
+    group contributes, with L and D from the oracle's own forward over all keys.
+
+    Returns (dK [n, d], dV [n, d]) in fp64.
+    """
+    hq = q.shape[1]
+    g = hq // k_pool.shape[2]
+    cu = _offsets(q_len)
+    dk = torch.zeros((len(keys), q.shape[2]), dtype=torch.float64)
+    dv = torch.zeros((len(keys), q.shape[2]), dtype=torch.float64)
+    groups = {}
+    for i, (b, kvh, pos) in enumerate(keys):
+        groups.setdefault((b, kvh), []).append((i, pos))
+    for (b, kvh), members in groups.items():
+        lq, lk = int(q_len[b]), int(kv_len[b])
+        kh = _seq_head(k_pool, block_table[b], lk, block_len, kvh)
+        vh = _seq_head(v_pool, block_table[b], lk, block_len, kvh)
+        idx = torch.tensor([pos for _, pos in members])
+        pos_all = torch.arange(lk)
+        for h in range(kvh * g, (kvh + 1) * g):
+            for t0 in range(0, lq, row_chunk):
+                t1 = min(lq, t0 + row_chunk)
+                qr = q[cu[b] + t0: cu[b] + t1, h].to(torch.float64)
+                dor = do[cu[b] + t0: cu[b] + t1, h].to(torch.float64)
+                vis = torch.tensor([visible_keys(lq, lk, t, causal) for t in range(t0, t1)])
+                mask = pos_all[None, :] < vis[:, None]
+                s = scale * (qr @ kh.T)
+                s = torch.where(mask, s, torch.full_like(s, -math.inf))
+                lse = torch.logsumexp(s, dim=1)
+                p_all = torch.exp(s - lse[:, None])
+                o = p_all @ vh
+                dlt = (dor * o).sum(dim=1)
+                p = p_all[:, idx]                              # [rows, n_sel]
+                dp = dor @ vh[idx].T
+                ds = p * (dp - dlt[:, None])
+                dvs = p.T @ dor
+                dks = scale * (ds.T @ qr)
+                for m, (i, _) in enumerate(members):
+                    dv[i] += dvs[m]
+                    dk[i] += dks[m]
+    return dk, dv

@@ -55,3 +55,38 @@ def test_backward_is_deterministic_in_dk_dv_and_close_in_dq():
     torch.cuda.synchronize()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])  # dK / dV: no atomics
     assert (a[0] - b[0]).abs().max().item() < 1e-4  # dQ: fp32 atomics, order may differ
+
+
+@pytest.mark.parametrize("name", ["shortq", "largest", "decode"])
+def test_backward_full_size_sampled(name):
+    """Full-size workloads: sampled dQ rows and sampled dK / dV keys against the oracle,
+    which computes each from its own forward (L, D) over all keys."""
+    import random
+
+    w = wl.WORKLOADS[name]
+    inp, run, out, lse = run_cuda(w)
+    g = torch.Generator(device="cuda").manual_seed(21)
+    dout = torch.randn(out.shape, generator=g, device="cuda", dtype=torch.float32).to(out.dtype)
+    dq, dk, dv = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+    torch.cuda.synchronize()
+    assert K.splitkv_device_status() == 0
+    rng = random.Random(3)
+    qc, kc, vc, tc, doc = inp.q.cpu(), inp.k_pool.cpu(), inp.v_pool.cpu(), inp.block_table.cpu(), dout.cpu()
+    args = (qc, kc, vc, tc, inp.q_len, inp.kv_len, w.block_len, w.causal, w.scale, doc)
+    rows = sorted({(b, rng.randrange(inp.q_len[b]), rng.randrange(w.Hq)) for b in rng.sample(range(w.B), min(w.B, 3))
+                   for _ in range(6)})
+    ref_dq = oracle.backward_rows(*args, rows=rows)
+    cu = [0]
+    for n in inp.q_len:
+        cu.append(cu[-1] + n)
+    got_dq = torch.stack([dq[cu[b] + t, h].cpu().double() for b, t, h in rows])
+    assert (got_dq - ref_dq).abs().max().item() <= TOL[w.dtype]
+    b0 = 0
+    kv = inp.kv_len[b0]
+    keys = [(b0, kvh, p) for kvh in (0, w.Hkv - 1) for p in (0, kv - 1, rng.randrange(kv), rng.randrange(kv))]
+    ref_dk, ref_dv = oracle.backward_keys(*args, keys=keys)
+    for i, (b, kvh, p) in enumerate(keys):
+        phys = int(tc[b, p // w.block_len])
+        off = p % w.block_len
+        assert (dk[phys, off, kvh].cpu().double() - ref_dk[i]).abs().max().item() <= TOL[w.dtype], ("dk", keys[i])
+        assert (dv[phys, off, kvh].cpu().double() - ref_dv[i]).abs().max().item() <= TOL[w.dtype], ("dv", keys[i])

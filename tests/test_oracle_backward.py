@@ -105,3 +105,21 @@ def test_planted_missing_delta_is_caught():
     good = oracle.attention_backward(**b, do=do, lse=lse, dlt=oracle.delta(o, do))
     bad = oracle.attention_backward(**b, do=do, lse=lse, dlt=torch.zeros_like(lse))
     assert (good[0] - bad[0]).abs().max() > 1e-3  # dQ changes when D is dropped
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_row_and_key_gradients_match_full(causal):
+    b = _random_batch(13, causal=causal, B=2)
+    do, (dq, dk, dv), _, _ = _grads(b, seed=5)
+    cu = [0, b["q_len"][0]]
+    rows = [(0, 0, 1), (1, b["q_len"][1] - 1, 3), (0, b["q_len"][0] - 1, 0)]
+    got = oracle.backward_rows(**b, do=do, rows=rows)
+    for i, (bb, t, h) in enumerate(rows):
+        assert torch.allclose(got[i], dq[cu[bb] + t, h], atol=1e-12, rtol=0)
+    keys = [(0, 0, 0), (1, 1, b["kv_len"][1] - 1), (1, 0, 2)]
+    gk, gv = oracle.backward_keys(**b, do=do, keys=keys, row_chunk=2)
+    for i, (bb, kvh, pos) in enumerate(keys):
+        blk, off = pos // b["block_len"], pos % b["block_len"]
+        phys = int(b["block_table"][bb, blk])
+        assert torch.allclose(gk[i], dk[phys, off, kvh], atol=1e-12, rtol=0)
+        assert torch.allclose(gv[i], dv[phys, off, kvh], atol=1e-12, rtol=0)
