@@ -206,9 +206,12 @@ def traffic_for(kernel_name, workload):
 def dcp_model(w):
     """Costs of the split-selection model for a context-parallel deployment of this
     workload: alpha = seconds per unit of block cost on one rank (4*d*Hq flops at
-    1200 TFLOP/s, the tensor-core kernel's measured rate), beta = seconds per partial
-    row exchanged and merged (Hq*(d+1)*4 bytes at 900 GB/s of NVLink)."""
-    return 4.0 * w.d * w.Hq / 1.2e15, w.Hq * (w.d + 1) * 4.0 / 0.9e12
+    1200 TFLOP/s, the tensor-core kernel's measured rate), gamma = seconds per K/V
+    token streamed (Hkv*d*2 elements at 5.7 TB/s, the decode kernel's measured rate),
+    beta = seconds per partial row exchanged and merged (Hq*(d+1)*4 bytes at 900 GB/s
+    of NVLink)."""
+    return (4.0 * w.d * w.Hq / 1.2e15, w.Hq * (w.d + 1) * 4.0 / 0.9e12,
+            w.Hkv * w.d * 2.0 * w.elem_bytes / 5.7e12)
 
 
 # -------------------------------------------------------------- our arm
@@ -231,10 +234,10 @@ def run_ours(args, dctx):
     kernel = {"auto": K.KERNEL_AUTO, "simt": K.KERNEL_SIMT, "decode": K.KERNEL_DECODE,
               "tc": K.KERNEL_TC}[args.kernel]
     inp = wl.make_inputs(w, device=f"cuda:{dev}")
-    alpha, beta = dcp_model(w)
+    alpha, beta, gamma = dcp_model(w)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
                            inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
-                           planner=args.planner, dcp_alpha=alpha, dcp_beta=beta)
+                           planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma)
     fused_one_launch = run.fused and run.kernel_used() == K.KERNEL_DECODE
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
@@ -254,6 +257,8 @@ def run_ours(args, dctx):
         if ev is not None:
             ev[1].record(stream)
         run.merge(out, lse)
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -261,8 +266,7 @@ def run_ours(args, dctx):
     if args.backward:
         return run_backward(args, dctx, w, inp, run, out, lse, acc)
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     sampler = ClockSampler(gpu_nvsmi_id(torch, dev), os.path.join(ROOT, f".bench_clocks_{dctx.rank}.csv"))
     sampler.start()
     dctx.barrier()
@@ -283,7 +287,8 @@ def run_ours(args, dctx):
     except OSError:
         pass
     local_s = t0.elapsed_time(t1) / 1e3
-    partial_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)  # the dominant kernel's launch
+    partial_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)  # the dominant kernel's launch
+    merge_ms = None if run.fused else sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
     t_max, units = aggregate(dctx, local_s, acc["kv_bytes"] * args.steps, device=f"cuda:{dev}")
     ms_per_step = 1e3 * t_max / args.steps
 
@@ -315,7 +320,7 @@ def run_ours(args, dctx):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     roof.update({"traffic": traffic_for(kname, w.name), "kernel": f"partial_{kname}",
-                 "kernel_ms": partial_ms, "peak_source": peak_src,
+                 "kernel_ms": partial_ms, "merge_ms": merge_ms, "peak_source": peak_src,
                  "algorithmic_per_launch": acc["partial_bytes"] if hbm_bound else acc["flops"]})
 
     value = units / t_max / 1e9  # GB/s of K/V read, all ranks

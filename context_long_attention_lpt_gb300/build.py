@@ -43,7 +43,8 @@ def _compile(nvcc, src, verbose):
     if src.endswith(".cu"):
         cmd += CUDA_FLAGS
     else:
-        cmd += ["-x", "c++"]
+        # host code: no FP contraction, so planner arithmetic rounds like the IEEE reference
+        cmd += ["-x", "c++", "-Xcompiler", "-ffp-contract=off"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

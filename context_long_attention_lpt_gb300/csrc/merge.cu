@@ -21,9 +21,39 @@ namespace splitkv {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kUnroll = 8;
+
+template <int N>
+struct Vec {
+  float v[N];
+};
+
+template <int N>
+__device__ __forceinline__ Vec<N> load_vec(const float* src) {
+  Vec<N> r;
+  if constexpr (N == 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+    r.v[0] = x.x; r.v[1] = x.y; r.v[2] = x.z; r.v[3] = x.w;
+  } else if constexpr (N == 2) {
+    const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+    r.v[0] = x.x; r.v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k) r.v[k] = __ldg(src + k);
+  }
+  return r;
+}
+
+// A zero weight (a shard with no visible key for this row) contributes nothing,
+// whatever its partial row holds.
+template <int N>
+__device__ __forceinline__ void accumulate(float (&acc)[N], float w, const Vec<N>& x) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) acc[k] = w != 0.f ? fmaf(w, x.v[k], acc[k]) : acc[k];
+}
 
 template <typename OutT, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 1)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  int64_t part_rows, const int32_t* __restrict__ work, int32_t B, int32_t total_q,
                  int32_t Hq, OutT* __restrict__ out, float* __restrict__ lse_out,
@@ -80,21 +110,25 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
       denom += my_w;
       const int n = min(32, p1 - base);
-      for (int k2 = 0; k2 < n; ++k2) {
+      // Eight partial rows per round: all eight loads are issued before the
+      // first FMA, so a warp has eight independent 512 B reads in flight.
+      int k2 = 0;
+      for (; k2 + kUnroll <= n; k2 += kUnroll) {
+        Vec<kPer> x[kUnroll];
+        float w[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          w[u] = __shfl_sync(0xffffffffu, my_w, k2 + u);
+          const int64_t r = __shfl_sync(0xffffffffu, my_row, k2 + u);
+          x[u] = load_vec<kPer>(o_part + r * D + lane * kPer);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) accumulate(acc, w[u], x[u]);
+      }
+      for (; k2 < n; ++k2) {
         const float w = __shfl_sync(0xffffffffu, my_w, k2);
         const int64_t r = __shfl_sync(0xffffffffu, my_row, k2);
-        if (w == 0.f) continue;
-        const float* src = o_part + r * D + lane * kPer;
-        if constexpr (kPer == 4) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(src));
-          acc[0] = fmaf(w, x.x, acc[0]);
-          acc[1] = fmaf(w, x.y, acc[1]);
-          acc[2] = fmaf(w, x.z, acc[2]);
-          acc[3] = fmaf(w, x.w, acc[3]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < kPer; ++k) acc[k] = fmaf(w, __ldg(src + k), acc[k]);
-        }
+        accumulate(acc, w, load_vec<kPer>(o_part + r * D + lane * kPer));
       }
     }
     denom = warp_sum(denom);

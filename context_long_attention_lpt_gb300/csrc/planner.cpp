@@ -97,6 +97,82 @@ extern "C" int splitkv_block_costs(const int32_t* q_len, const int32_t* kv_len, 
   return SPLITKV_OK;
 }
 
+namespace {
+
+// Longest first; equal costs keep ascending block index.  When every cost and
+// index fits in 32 bits the pair is packed into one 64-bit key (complemented
+// cost high, index low) so the sort compares plain integers.
+void lpt_order(const int64_t* block_cost, int64_t n_blocks, std::vector<int64_t>& order) {
+  order.resize(static_cast<size_t>(n_blocks));
+  int64_t max_cost = 0;
+  for (int64_t g = 0; g < n_blocks; ++g) max_cost = std::max(max_cost, block_cost[g]);
+  if (max_cost <= 0xffffffffLL && n_blocks <= 0xffffffffLL) {
+    std::vector<uint64_t> key(static_cast<size_t>(n_blocks));
+    for (int64_t g = 0; g < n_blocks; ++g)
+      key[g] = ((0xffffffffull - static_cast<uint64_t>(block_cost[g])) << 32) | static_cast<uint64_t>(g);
+    std::sort(key.begin(), key.end());
+    for (int64_t i = 0; i < n_blocks; ++i) order[i] = static_cast<int64_t>(key[i] & 0xffffffffull);
+    return;
+  }
+  for (int64_t g = 0; g < n_blocks; ++g) order[g] = g;
+  std::sort(order.begin(), order.end(), [&](int64_t x, int64_t y) {
+    return block_cost[x] != block_cost[y] ? block_cost[x] > block_cost[y] : x < y;
+  });
+}
+
+// Each block in `order` goes to the least-loaded shard, the smallest
+// (load, id) pair: a binary min-heap on that pair.  Shards 0..n-1 with zero
+// load already form a valid heap (a parent's index, hence id, is lower).  When
+// the total cost leaves room, the pair is packed as load * 2^bits + id into one
+// unsigned key, which orders exactly like the pair.
+template <typename Key, typename Less, typename Add, typename IdOf>
+void sift_assign(const std::vector<int64_t>& order, const int64_t* block_cost, int32_t n, std::vector<Key>& heap,
+                 Less less, Add add, IdOf id_of, int32_t* shard_of_block) {
+  for (int64_t g : order) {
+    shard_of_block[g] = id_of(heap[0]);
+    const Key top = add(heap[0], block_cost[g]);
+    int32_t i = 0;
+    for (;;) {
+      const int32_t l = 2 * i + 1, r = l + 1;
+      if (l >= n) break;
+      const int32_t m = (r < n && less(heap[r], heap[l])) ? r : l;
+      if (!less(heap[m], top)) break;
+      heap[i] = heap[m];
+      i = m;
+    }
+    heap[i] = top;
+  }
+}
+
+void lpt_assign_sorted(const std::vector<int64_t>& order, const int64_t* block_cost, int32_t n_shards,
+                       int32_t* shard_of_block, int64_t* shard_load) {
+  int bits = 1;
+  while ((int64_t{1} << bits) < n_shards) ++bits;
+  uint64_t total = 0;
+  for (int64_t g : order) total += static_cast<uint64_t>(block_cost[g]);
+  if (total < (uint64_t{1} << (63 - bits))) {
+    const uint64_t mask = (uint64_t{1} << bits) - 1;
+    std::vector<uint64_t> heap(static_cast<size_t>(n_shards));
+    for (int32_t k = 0; k < n_shards; ++k) heap[k] = static_cast<uint64_t>(k);
+    sift_assign(
+        order, block_cost, n_shards, heap, [](uint64_t x, uint64_t y) { return x < y; },
+        [bits](uint64_t x, int64_t c) { return x + (static_cast<uint64_t>(c) << bits); },
+        [mask](uint64_t x) { return static_cast<int32_t>(x & mask); }, shard_of_block);
+    for (int32_t k = 0; k < n_shards; ++k) shard_load[heap[k] & mask] = static_cast<int64_t>(heap[k] >> bits);
+    return;
+  }
+  using Slot = std::pair<int64_t, int32_t>;
+  std::vector<Slot> heap(static_cast<size_t>(n_shards));
+  for (int32_t k = 0; k < n_shards; ++k) heap[k] = {0, k};
+  sift_assign(
+      order, block_cost, n_shards, heap, [](const Slot& x, const Slot& y) { return x < y; },
+      [](const Slot& x, int64_t c) { return Slot{x.first + c, x.second}; },
+      [](const Slot& x) { return x.second; }, shard_of_block);
+  for (int32_t k = 0; k < n_shards; ++k) shard_load[heap[k].second] = heap[k].first;
+}
+
+}  // namespace
+
 extern "C" int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t n_shards,
                             int32_t* shard_of_block, int64_t* shard_load) {
   if (n_blocks < 0 || (n_blocks > 0 && (!block_cost || !shard_of_block)))
@@ -106,29 +182,9 @@ extern "C" int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t
   for (int64_t g = 0; g < n_blocks; ++g)
     if (block_cost[g] < 0) return fail(SPLITKV_ERR_INVALID, "negative cost at block %lld", (long long)g);
 
-  // Longest first; equal costs keep ascending block index.
-  std::vector<int64_t> order(static_cast<size_t>(n_blocks));
-  for (int64_t g = 0; g < n_blocks; ++g) order[g] = g;
-  std::sort(order.begin(), order.end(), [&](int64_t x, int64_t y) {
-    return block_cost[x] != block_cost[y] ? block_cost[x] > block_cost[y] : x < y;
-  });
-
-  // Least-loaded shard = smallest (load, id): a min-heap on that pair.
-  using Slot = std::pair<int64_t, int32_t>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int32_t s = 0; s < n_shards; ++s) heap.push({0, s});
-  for (int64_t g : order) {
-    Slot top = heap.top();
-    heap.pop();
-    shard_of_block[g] = top.second;
-    top.first += block_cost[g];
-    heap.push(top);
-  }
-  for (int32_t s = 0; s < n_shards; ++s) shard_load[s] = 0;
-  while (!heap.empty()) {
-    shard_load[heap.top().second] = heap.top().first;
-    heap.pop();
-  }
+  std::vector<int64_t> order;
+  lpt_order(block_cost, n_blocks, order);
+  lpt_assign_sorted(order, block_cost, n_shards, shard_of_block, shard_load);
   splitkv::clear_error();
   return SPLITKV_OK;
 }
@@ -279,16 +335,18 @@ extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, i
 }
 
 extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
-                                int32_t causal, int32_t max_shards, double alpha, double beta,
+                                int32_t causal, int32_t max_shards, double alpha, double beta, double gamma,
                                 int32_t* shard_of_block, int64_t n_blocks, int64_t* shard_load,
                                 int32_t* n_shards_used, double* modeled_time) {
   // Split selection that models attention completion together with the reduction
   // that depends on it (LiquidCP abstract: MegaDCP).  For every shard count s the
   // blocks are planned with the same LPT rule; the shards run concurrently, so
-  // attention completes with the most loaded one, and the reduction combines one
+  // attention completes with the slowest one - compute (alpha per unit of block
+  // cost) plus K/V streaming (gamma per token) - and the reduction combines one
   // partial row per (shard, sequence) pair and query token:
-  //     T(s) = alpha * max_load(s) + beta * partial_rows(s)
-  // The smallest s reaching the least T wins.
+  //     T(s) = max_k (alpha * load_k + gamma * tokens_k) + beta * partial_rows(s)
+  // (each product rounded on its own: this file is compiled without FP
+  // contraction).  The smallest s reaching the least T wins.
   int st = 0;
   if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
   if (max_shards <= 0 || !shard_of_block || !shard_load || !n_shards_used || !modeled_time)
@@ -297,21 +355,52 @@ extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int
   st = splitkv_block_costs(q_len, kv_len, B, block_len, causal, costs.data(), n_blocks);
   if (st != SPLITKV_OK) return st;
   std::vector<int32_t> seq_of(static_cast<size_t>(n_blocks));
+  std::vector<int64_t> tokens(static_cast<size_t>(n_blocks));
   {
     int64_t g = 0;
     for (int32_t b = 0; b < B; ++b)
-      for (int64_t j = 0; j < (static_cast<int64_t>(kv_len[b]) + block_len - 1) / block_len; ++j) seq_of[g++] = b;
+      for (int64_t j = 0; j < (static_cast<int64_t>(kv_len[b]) + block_len - 1) / block_len; ++j) {
+        seq_of[g] = b;
+        tokens[g++] = std::min<int64_t>(block_len, kv_len[b] - j * block_len);
+      }
   }
   std::vector<int32_t> sob(static_cast<size_t>(n_blocks)), best_sob;
   std::vector<int64_t> load(static_cast<size_t>(max_shards)), best_load;
   std::vector<uint8_t> held(static_cast<size_t>(max_shards));
+  std::vector<int64_t> shard_tok(static_cast<size_t>(max_shards));
   int32_t best_s = 0;
   double best_t = 0.0;
-  for (int32_t s = 1; s <= max_shards; ++s) {
-    st = splitkv_plan(costs.data(), n_blocks, s, sob.data(), load.data());
-    if (st != SPLITKV_OK) return st;
-    int64_t max_load = 0;
-    for (int32_t k = 0; k < s; ++k) max_load = std::max(max_load, load[k]);
+  std::vector<int64_t> order;
+  lpt_order(costs.data(), n_blocks, order);  // the LPT order does not depend on s
+
+  // Shard counts are tried from the largest down, so the first smaller s whose
+  // lower bound exceeds the best T found ends the search: every shard count
+  // below it has a larger bound.  The bound holds for non-negative
+  // coefficients: the slowest shard is at least the mean (alpha*C + gamma*N)/s
+  // over all cost C and tokens N, and each sequence with keys adds at least one
+  // partial row per query token.  The relative margin covers the rounding of
+  // both sides, so the chosen s is the one the exhaustive search picks.
+  const bool prune = alpha >= 0.0 && beta >= 0.0 && gamma >= 0.0;
+  int64_t cost_sum = 0, tok_sum = 0, rows_min = 0;
+  for (int64_t g = 0; g < n_blocks; ++g) {
+    cost_sum += costs[g];
+    tok_sum += tokens[g];
+  }
+  for (int32_t b = 0; b < B; ++b)
+    if (kv_len[b] > 0) rows_min += q_len[b];
+  const double att_sum = alpha * static_cast<double>(cost_sum) + gamma * static_cast<double>(tok_sum);
+  for (int32_t s = max_shards; s >= 1; --s) {
+    if (prune && best_s != 0 && best_t > 0.0 &&
+        att_sum / s + beta * static_cast<double>(rows_min) > best_t * (1.0 + 1e-9))
+      break;
+    lpt_assign_sorted(order, costs.data(), s, sob.data(), load.data());
+    std::fill(shard_tok.begin(), shard_tok.begin() + s, 0);
+    for (int64_t g = 0; g < n_blocks; ++g) shard_tok[sob[g]] += tokens[g];
+    double t_att = 0.0;
+    for (int32_t k = 0; k < s; ++k) {
+      const double tk = alpha * static_cast<double>(load[k]) + gamma * static_cast<double>(shard_tok[k]);
+      if (k == 0 || tk > t_att) t_att = tk;
+    }
     // partial rows: blocks are sequence-major, so one pass with a per-sequence shard mask
     int64_t rows = 0;
     for (int64_t g = 0; g < n_blocks;) {
@@ -325,8 +414,8 @@ extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int
         }
       rows += static_cast<int64_t>(distinct) * q_len[b];
     }
-    const double t = alpha * static_cast<double>(max_load) + beta * static_cast<double>(rows);
-    if (best_s == 0 || t < best_t) {
+    const double t = t_att + beta * static_cast<double>(rows);
+    if (best_s == 0 || t <= best_t) {  // s is decreasing: a tie goes to the smaller s
       best_s = s;
       best_t = t;
       best_sob = sob;

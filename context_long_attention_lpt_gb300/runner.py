@@ -20,7 +20,7 @@ from . import splitkv as _k
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
                  device="cuda", kernel=_k.KERNEL_AUTO, fused=False, planner="lpt", dcp_alpha=1.0,
-                 dcp_beta=0.0):
+                 dcp_beta=0.0, dcp_gamma=0.0):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -35,16 +35,18 @@ class SplitKVAttention:
         if planner not in ("lpt", "dcp"):
             raise ValueError("planner must be 'lpt' or 'dcp'")
         self.planner = planner
-        self.dcp_alpha, self.dcp_beta = float(dcp_alpha), float(dcp_beta)
+        self.dcp_alpha, self.dcp_beta, self.dcp_gamma = float(dcp_alpha), float(dcp_beta), float(dcp_gamma)
         self.n_shards_used = self.n_shards
         self._tickets = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
         self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
         self._kv_len_np = np.asarray(self.kv_len, dtype=np.int32)
-        self._work_host = None
+        # pinned staging buffers for the work list, used in turn, so planning the
+        # next batches on the host runs up to len(ring) uploads ahead of the device
+        self._ring = [[None, None] for _ in range(3)]  # [pinned buffer, upload-done event]
+        self._ring_next = 0
         self._work_dev = None
-        self._work_copied = None
         self._o_part = None
         self._lse_part = None
         self.plan()
@@ -59,19 +61,22 @@ class SplitKVAttention:
         else:
             self.n_shards_used, self.shard_of_block, self.shard_load, self.modeled_time = _k.splitkv_plan_dcp(
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
-                self.dcp_beta)
+                self.dcp_beta, self.dcp_gamma)
         work, self.n_items, self.part_rows = _k.splitkv_build_work(
             self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
             self.n_shards)
-        if self._work_copied is not None:
-            self._work_copied.synchronize()  # the previous upload has left the pinned buffer
-        if self._work_host is None or self._work_host.numel() < work.size:
-            self._work_host = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
+        slot = self._ring[self._ring_next]
+        self._ring_next = (self._ring_next + 1) % len(self._ring)
+        if slot[1] is not None:
+            slot[1].synchronize()  # this buffer's last upload has left it
+        if slot[0] is None or slot[0].numel() < work.size:
+            slot[0] = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
+        if self._work_dev is None or self._work_dev.numel() < work.size:
             self._work_dev = torch.empty(work.size, dtype=torch.int32, device=self.device)
-        self._work_host[: work.size].copy_(torch.from_numpy(work))
-        self._work_dev[: work.size].copy_(self._work_host[: work.size], non_blocking=True)
-        self._work_copied = torch.cuda.Event()
-        self._work_copied.record()
+        slot[0][: work.size].copy_(torch.from_numpy(work))
+        self._work_dev[: work.size].copy_(slot[0][: work.size], non_blocking=True)
+        slot[1] = torch.cuda.Event()
+        slot[1].record()
         self.work_host = work
         if self._o_part is None or self._o_part.shape[0] < self.part_rows:
             self._o_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32,

@@ -27,8 +27,8 @@ _SIGNATURES = {
     "splitkv_num_blocks": (_i64, [_p, _i32, _i32]),
     "splitkv_block_costs": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _i64]),
     "splitkv_plan": (ctypes.c_int, [_p, _i64, _i32, _p, _p]),
-    "splitkv_plan_dcp": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, ctypes.c_double, ctypes.c_double, _p,
-                                        _i64, _p, _p, _p]),
+    "splitkv_plan_dcp": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_double, _p, _i64, _p, _p, _p]),
     "splitkv_work_words": (_i64, [_i64, _i32]),
     "splitkv_build_work": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _p, _i64, _p, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
@@ -126,7 +126,7 @@ def splitkv_plan(block_cost, n_shards):
     return sob, load
 
 
-def splitkv_plan_dcp(q_len, kv_len, block_len, causal, max_shards, alpha, beta):
+def splitkv_plan_dcp(q_len, kv_len, block_len, causal, max_shards, alpha, beta, gamma=0.0):
     """Returns (n_shards_used, shard_of_block, shard_load[max_shards], modeled_time)."""
     q, kv = _np(q_len, np.int32), _np(kv_len, np.int32)
     n = splitkv_num_blocks(kv, block_len)
@@ -135,7 +135,8 @@ def splitkv_plan_dcp(q_len, kv_len, block_len, causal, max_shards, alpha, beta):
     used = ctypes.c_int32(0)
     t = ctypes.c_double(0.0)
     _check("splitkv_plan_dcp", lib().splitkv_plan_dcp(_ptr(q), _ptr(kv), len(q), block_len, int(bool(causal)),
-                                                     max_shards, float(alpha), float(beta), _ptr(sob), n,
+                                                     max_shards, float(alpha), float(beta), float(gamma),
+                                                     _ptr(sob), n,
                                                      _ptr(load), ctypes.byref(used), ctypes.byref(t)))
     return used.value, sob, load, t.value
 

@@ -86,16 +86,18 @@ int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t n_shards,
  * abstract, PaperTrail: its MegaDCP selects history-KV splits this way; the
  * abstract gives no formula, this is the plainest reading).  For every shard
  * count s in 1..max_shards the blocks are planned with splitkv_plan's LPT rule;
- * attention completes with the most loaded shard and the reduction combines one
- * partial row per (shard, sequence) pair and query token, so
- *     T(s) = alpha * max_load(s) + beta * partial_rows(s)      (IEEE double)
- * where partial_rows(s) = sum over distinct (shard, sequence) pairs of q_len.
+ * attention completes with the slowest shard - alpha per unit of its block cost
+ * plus gamma per K/V token it streams - and the reduction combines one partial
+ * row per (shard, sequence) pair and query token, so
+ *     T(s) = max_k (alpha*load_k + gamma*tokens_k) + beta*partial_rows(s)
+ * (IEEE double, each product rounded separately) where partial_rows(s) = sum
+ * over distinct (shard, sequence) pairs of q_len.
  * The smallest s reaching the least T is chosen.  Out (host): shard_of_block
  * [n_blocks] (ids < *n_shards_used), shard_load[max_shards] (0 past the chosen
  * count), *n_shards_used, *modeled_time.  alpha: time per unit of block cost on
  * one shard; beta: time per partial row to merge (any consistent unit). */
 int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
-                     int32_t causal, int32_t max_shards, double alpha, double beta,
+                     int32_t causal, int32_t max_shards, double alpha, double beta, double gamma,
                      int32_t* shard_of_block, int64_t n_blocks, int64_t* shard_load,
                      int32_t* n_shards_used, double* modeled_time);
 

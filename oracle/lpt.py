@@ -94,7 +94,18 @@ def partial_rows(shard_of_block, q_len, kv_len, block_len):
     return sum(int(q_len[b]) for _, b in pairs)
 
 
-def dcp_select(q_len, kv_len, block_len, causal, max_shards, alpha, beta):
+def shard_tokens(shard_of_block, kv_len, block_len, n_shards):
+    """K/V tokens each shard streams (the keys of its blocks)."""
+    tok = [0] * n_shards
+    g = 0
+    for lk in kv_len:
+        for j in range(-(-int(lk) // block_len)):
+            tok[shard_of_block[g]] += min(block_len, int(lk) - j * block_len)
+            g += 1
+    return tok
+
+
+def dcp_select(q_len, kv_len, block_len, causal, max_shards, alpha, beta, gamma=0.0):
     """Split selection that models attention completion together with its reduction.
 
     After the LiquidCP abstract (PaperTrail, arXiv 2611.04401): MegaDCP picks
@@ -102,17 +113,20 @@ def dcp_select(q_len, kv_len, block_len, causal, max_shards, alpha, beta):
     reductions that depend on it.  The abstract gives no formula; the reading
     taken here: for every shard count s in 1..max_shards, plan the blocks with
     the cost-aware LPT rule onto s shards; the shards run concurrently, so
-    attention completes with the most loaded shard, and the reduction then has
-    to combine one partial row per (shard, sequence) pair and query token:
-        T(s) = alpha * max_load(s) + beta * partial_rows(s)
-    (evaluated in IEEE double exactly in this order).  The smallest s reaching
-    the least T wins.  Returns (s, shard_of_block, load, T(s)).
+    attention completes with the slowest shard - its compute (alpha per unit
+    of block cost) plus its K/V streaming (gamma per token) - and the reduction
+    then combines one partial row per (shard, sequence) pair and query token:
+        T(s) = max_k (alpha * load_k + gamma * tokens_k) + beta * partial_rows(s)
+    (IEEE double, each product rounded, in exactly this order).  The smallest s
+    reaching the least T wins.  Returns (s, shard_of_block, load, T(s)).
     """
     costs = block_costs(q_len, kv_len, block_len, causal)
     best = None
     for s in range(1, max_shards + 1):
         sob, load = lpt_assign(costs, s)
-        t = float(alpha) * float(max(load)) + float(beta) * float(partial_rows(sob, q_len, kv_len, block_len))
+        tok = shard_tokens(sob, kv_len, block_len, s)
+        t_att = max(float(alpha) * float(load[k]) + float(gamma) * float(tok[k]) for k in range(s))
+        t = t_att + float(beta) * float(partial_rows(sob, q_len, kv_len, block_len))
         if best is None or t < best[3]:
             best = (s, sob, load, t)
     return best

@@ -207,14 +207,15 @@ def test_fused_decode_full_size_and_ragged():
     assert int(run2.tickets.abs().sum()) == 0
 
 
-@pytest.mark.parametrize("name,beta", [("varlen_small", 50.0), ("decode_small", 1e9), ("shortq_small", 3.0)])
-def test_dcp_plan_through_the_kernels(name, beta):
+@pytest.mark.parametrize("name,beta,gamma", [("varlen_small", 50.0, 0.0), ("decode_small", 1e9, 0.0),
+                                             ("shortq_small", 3.0, 0.0), ("varlen_small", 40.0, 0.5)])
+def test_dcp_plan_through_the_kernels(name, beta, gamma):
     """The split-selection planner's plan (fewer shards than offered) runs through the same kernels."""
     w = SMALL[name]
     inp = wl.make_inputs(w, device="cuda", poison_tail=True)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
-                           inp.q.dtype, planner="dcp", dcp_alpha=1.0, dcp_beta=beta)
-    ref = oracle.dcp_select(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, 1.0, beta)
+                           inp.q.dtype, planner="dcp", dcp_alpha=1.0, dcp_beta=beta, dcp_gamma=gamma)
+    ref = oracle.dcp_select(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, 1.0, beta, gamma)
     assert run.n_shards_used == ref[0] and run.shard_of_block.tolist() == ref[1]
     out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
     torch.cuda.synchronize()

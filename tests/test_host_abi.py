@@ -185,12 +185,13 @@ def test_work_buffer_too_small_is_capacity_error(k):
 
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
-@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.0, 1e9), (1.0, 100.0), (0.25, 3.5)])
-def test_dcp_selection_matches_oracle(k, name, alpha, beta):
+@pytest.mark.parametrize("alpha,beta,gamma", [(1.0, 0.0, 0.0), (1.0, 1e9, 0.0), (1.0, 100.0, 0.0),
+                                              (0.25, 3.5, 0.0), (0.1, 3.0, 7.3), (1.3e-11, 1.9e-8, 7.2e-10)])
+def test_dcp_selection_matches_oracle(k, name, alpha, beta, gamma):
     w = wl.WORKLOADS[name]
     q, kv = wl.lengths(w)
-    s, sob, load, t = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta)
-    rs, rsob, rload, rt = oracle.dcp_select(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta)
+    s, sob, load, t = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta, gamma)
+    rs, rsob, rload, rt = oracle.dcp_select(q, kv, w.block_len, w.causal, w.n_shards, alpha, beta, gamma)
     assert (s, sob.tolist(), load[:s].tolist(), t) == (rs, rsob, rload, rt)
     assert (load[s:] == 0).all()
 
@@ -203,10 +204,10 @@ def test_fuzz_dcp_selection(k):
         kv = [qq + rng.randint(0, 200) for qq in q]
         bl = rng.choice([4, 16, 32])
         S = rng.randint(1, 8)
-        a, b = rng.choice([0.0, 1.0, 2.5]), rng.choice([0.0, 0.5, 7.0, 1e6])
+        a, b, c = rng.choice([0.0, 1.0, 2.5]), rng.choice([0.0, 0.5, 7.0, 1e6]), rng.choice([0.0, 0.3, 11.0])
         causal = rng.random() < 0.5
-        got = k.splitkv_plan_dcp(q, kv, bl, causal, S, a, b)
-        ref = oracle.dcp_select(q, kv, bl, causal, S, a, b)
+        got = k.splitkv_plan_dcp(q, kv, bl, causal, S, a, b, c)
+        ref = oracle.dcp_select(q, kv, bl, causal, S, a, b, c)
         assert (got[0], got[1].tolist(), got[3]) == (ref[0], ref[1], ref[3]), case
 
 
