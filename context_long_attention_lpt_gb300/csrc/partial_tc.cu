@@ -9,7 +9,7 @@
 // One CTA = one (work item, K/V head, 256 query rows) unit, split into two
 // 128-row query tiles A and B that share every K/V tile.  Row r of the unit is
 // token r / G, query head kvh*G + r % G.  Warp roles (384 threads, three
-// warpgroups; the softmax groups take 224 registers a thread, the third 56):
+// warpgroups; the softmax groups take 216 registers a thread, the third 72):
 //   warps 0-3  softmax + epilogue of tile A: thread i owns row i (TMEM lane i);
 //   warps 4-7  the same for tile B;
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
@@ -53,9 +53,9 @@ constexpr int kN = 128;       // keys per KV tile
 constexpr int kStages = 2;    // K and V ring depth
 constexpr int kThreads = 384;
 // Register split: launched at 168 a thread (384 x 168 = 64512), the two softmax
-// warpgroups grow to 224 and the producer / MMA warpgroup shrinks to 56:
-// 2 x 128 x 224 + 128 x 56 = 64512 (per SM sub-partition 224 + 224 + 56 <= 512).
-constexpr int kRegsSoftmax = 224, kRegsOther = 56;
+// warpgroups grow to 216 and the producer / MMA warpgroup shrinks to 72:
+// 2 x 128 x 216 + 128 x 72 = 64512 (per SM sub-partition 216 + 216 + 72 <= 512).
+constexpr int kRegsSoftmax = 216, kRegsOther = 72;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
@@ -239,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
+    // One thread runs this role: it alone waits on the barriers and issues
+    // every tcgen05.mma / commit, so no wait or vote costs a warp round trip
+    // between bursts of MMAs (the tensor pipe drains during such gaps).
+    if (lane == 0) {
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
     const int nx = has_b ? 2 : 1;
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const tc::Desc desc_k0 = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
     const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
     constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
-    // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
+    // S_X = Q_X K^T for KV tile t (K in stage t % kStages)
     auto issue_s = [&](int x, int32_t t) {
       const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
       const uint32_t d_col = tmem + col_s(x);
@@ -283,78 +287,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
     };
-    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
+    bool ok = ptx::mbar_wait(&bar->q_full, 0);
     int32_t nv_cur = 0, nv_next = 0;
     bool has_cur = ok && next_tile(&nv_cur);
     int32_t t = 0;
     if (has_cur) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
+      ok = ptx::mbar_wait(&bar->k_full[0], 0);
       tc::fence_after_sync();
-      if (ok && lane == 0) {
+      if (ok) {
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
         tc::commit(&bar->k_empty[0]);
       }
-      __syncwarp();
     }
     while (has_cur && ok) {
       const bool has_next = next_tile(&nv_next);
       const int vs = t % kStages;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1))) { ok = false; break; }
+      if (!ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1)) { ok = false; break; }
       uint8_t* vtile = sv + vs * kTileBytes;
       const int ksteps = (nv_cur + 15) >> 4;
       if (nv_cur < ksteps * 16) {
         // zero the V rows of keys past the end inside the last 16-key step
-        for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
-          const int cc = lane & 15;
-          uint4* dst = reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128) + (cc & 7);
-          *dst = make_uint4(0, 0, 0, 0);
-        }
+        for (int r = nv_cur; r < ksteps * 16; ++r)
+          for (int cc = 0; cc < 16; ++cc)
+            reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128)[cc & 7] = make_uint4(0, 0, 0, 0);
         tc::fence_proxy_async_smem();
-        __syncwarp();
       }
       const uint32_t voff = vs * kTile16;
-      if (has_next &&
-          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
+      if (has_next && !ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1)) {
         ok = false;
         break;
       }
       for (int x = 0; x < nx; ++x) {
         // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[x], t & 1))) {
+        if (!ptx::mbar_wait(&bar->p_full[x], t & 1)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (lane == 0) {
-          const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
-          if (ksteps == kN / 16 && t > 0) {
+        const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
+        if (ksteps == kN / 16 && t > 0) {
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
-          } else {
-            for (int kk = 0; kk < ksteps; ++kk)
-              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
-                              (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::commit(&bar->o_done[x]);
-          if (x == nx - 1) tc::commit(&bar->v_empty[vs]);
-          if (has_next) {
-            issue_s(x, t + 1);
-            if (x == nx - 1) tc::commit(&bar->k_empty[(t + 1) % kStages]);
-          }
+          for (int kk = 0; kk < kN / 16; ++kk)
+            tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
+        } else {
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
+                            (t > 0 || kk > 0) ? 1u : 0u);
         }
-        __syncwarp();
+        tc::commit(&bar->o_done[x]);
+        if (x == nx - 1) tc::commit(&bar->v_empty[vs]);
+        if (has_next) {
+          issue_s(x, t + 1);
+          if (x == nx - 1) tc::commit(&bar->k_empty[(t + 1) % kStages]);
+        }
       }
       if (!ok) break;
       ++t;
       has_cur = has_next;
       nv_cur = nv_next;
     }
-    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
-    // all MMAs issued by this warp have completed before TMEM is released
-    if (lane == 0) tc::commit(&bar->drain);
+    if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
+    // all MMAs issued by this thread have completed before TMEM is released
+    tc::commit(&bar->drain);
+    if (!ptx::mbar_wait(&bar->drain, 0)) atomicOr(a.status, ptx::kStatusTimeout);
+    }
     __syncwarp();
-    if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   }
   } else {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
