@@ -70,8 +70,10 @@ __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 384u : 128u; }
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t k_full[kStages], v_full[kStages];
+  // kv_free[j % kStages] completes the j-th release: K tile j and V tile j-1
+  // have been consumed by their MMAs (one commit after S(j), issued after PV(j-1))
+  uint64_t kv_free[kStages];
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   uint64_t drain;
   uint32_t tmem_base;
@@ -170,9 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bar->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bar->k_full[s], 1);
-      ptx::mbar_init(&bar->k_empty[s], 1);
       ptx::mbar_init(&bar->v_full[s], 1);
-      ptx::mbar_init(&bar->v_empty[s], 1);
+      ptx::mbar_init(&bar->kv_free[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(&bar->s_full[x], 1);
@@ -218,12 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t off = 0; off < n; off += kN, ++t) {
           const int32_t tok = phys * a.block_len + off;
           const int s = t % kStages;
-          const uint32_t ph = ((t / kStages) & 1) ^ 1;
-          if (t >= kStages && !ptx::mbar_wait(&bar->k_empty[s], ph)) { ok = false; break; }
+          // K(t) reuses K(t - kStages)'s slot: release t - kStages; V(t) reuses
+          // V(t - kStages)'s slot: release t - kStages + 1
+          if (t >= kStages && !ptx::mbar_wait(&bar->kv_free[s], ((t - kStages) / kStages) & 1)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&bar->k_full[s], kTileBytes);
           ptx::tma_load_3d(sk + s * kTileBytes, &tmap_k, 0, kvh, tok, &bar->k_full[s]);
           ptx::tma_load_3d(sk + s * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->k_full[s]);
-          if (t >= kStages && !ptx::mbar_wait(&bar->v_empty[s], ph)) { ok = false; break; }
+          if (t >= kStages &&
+              !ptx::mbar_wait(&bar->kv_free[(t + 1) % kStages], ((t - kStages + 1) / kStages) & 1)) {
+            ok = false;
+            break;
+          }
           ptx::mbar_arrive_expect_tx(&bar->v_full[s], kTileBytes);
           ptx::tma_load_3d(sv + s * kTileBytes, &tmap_v, 0, kvh, tok, &bar->v_full[s]);
           ptx::tma_load_3d(sv + s * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->v_full[s]);
@@ -239,10 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    // One thread runs this role: it alone waits on the barriers and issues
-    // every tcgen05.mma / commit, so no wait or vote costs a warp round trip
-    // between bursts of MMAs (the tensor pipe drains during such gaps).
-    if (lane == 0) {
+    // The whole warp walks the tiles and waits on the barriers (a warp-wide
+    // wait is cheaper than one lane's divergent wait); lane 0 issues every
+    // tcgen05.mma and commit.  Commits are kept to three a tile: the tensor
+    // pipe drains while this thread is busy with anything but MMAs.
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
     const int nx = has_b ? 2 : 1;
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const tc::Desc desc_k0 = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
     const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
     constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
-    // S_X = Q_X K^T for KV tile t (K in stage t % kStages)
+    // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
     auto issue_s = [&](int x, int32_t t) {
       const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
       const uint32_t d_col = tmem + col_s(x);
@@ -287,71 +293,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
     };
-    bool ok = ptx::mbar_wait(&bar->q_full, 0);
+    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
     int32_t nv_cur = 0, nv_next = 0;
     bool has_cur = ok && next_tile(&nv_cur);
     int32_t t = 0;
     if (has_cur) {
-      ok = ptx::mbar_wait(&bar->k_full[0], 0);
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
       tc::fence_after_sync();
-      if (ok) {
+      if (ok && lane == 0) {
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
-        tc::commit(&bar->k_empty[0]);
+        tc::commit(&bar->kv_free[0]);  // release 0: K(0)
       }
+      __syncwarp();
     }
     while (has_cur && ok) {
       const bool has_next = next_tile(&nv_next);
       const int vs = t % kStages;
-      if (!ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1))) { ok = false; break; }
       uint8_t* vtile = sv + vs * kTileBytes;
       const int ksteps = (nv_cur + 15) >> 4;
       if (nv_cur < ksteps * 16) {
         // zero the V rows of keys past the end inside the last 16-key step
-        for (int r = nv_cur; r < ksteps * 16; ++r)
-          for (int cc = 0; cc < 16; ++cc)
-            reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128)[cc & 7] = make_uint4(0, 0, 0, 0);
+        for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
+          const int cc = lane & 15;
+          uint4* dst = reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128) + (cc & 7);
+          *dst = make_uint4(0, 0, 0, 0);
+        }
         tc::fence_proxy_async_smem();
+        __syncwarp();
       }
       const uint32_t voff = vs * kTile16;
-      if (has_next && !ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1)) {
+      if (has_next &&
+          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
         ok = false;
         break;
       }
       for (int x = 0; x < nx; ++x) {
         // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
-        if (!ptx::mbar_wait(&bar->p_full[x], t & 1)) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[x], t & 1))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
-        if (ksteps == kN / 16 && t > 0) {
+        if (lane == 0) {
+          const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
+          if (ksteps == kN / 16 && t > 0) {
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk)
-            tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
-        } else {
-          for (int kk = 0; kk < ksteps; ++kk)
-            tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
-                            (t > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk)
+              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
+          } else {
+            for (int kk = 0; kk < ksteps; ++kk)
+              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
+                              (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          // While tiles follow, the next S_X commit also covers this PV_X (a
+          // commit tracks every earlier MMA of this thread); only the last PV
+          // needs its own signal, for the epilogue.
+          if (has_next)
+            issue_s(x, t + 1);
+          else
+            tc::commit(&bar->o_done[x]);
+          if (x == nx - 1) tc::commit(&bar->kv_free[(t + 1) % kStages]);  // release t+1: K(t+1), V(t)
         }
-        tc::commit(&bar->o_done[x]);
-        if (x == nx - 1) tc::commit(&bar->v_empty[vs]);
-        if (has_next) {
-          issue_s(x, t + 1);
-          if (x == nx - 1) tc::commit(&bar->k_empty[(t + 1) % kStages]);
-        }
+        __syncwarp();
       }
       if (!ok) break;
       ++t;
       has_cur = has_next;
       nv_cur = nv_next;
     }
-    if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
-    // all MMAs issued by this thread have completed before TMEM is released
-    tc::commit(&bar->drain);
-    if (!ptx::mbar_wait(&bar->drain, 0)) atomicOr(a.status, ptx::kStatusTimeout);
-    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    // all MMAs issued by this warp have completed before TMEM is released
+    if (lane == 0) tc::commit(&bar->drain);
     __syncwarp();
+    if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   }
   } else {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -421,10 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold P_{t-1} V_{t-1} before it is rescaled (need implies t > 0);
-          // PV_{t-2} was observed before P_{t-1} was published, so this wait is exact
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) { ok = false; break; }
-          tc::fence_after_sync();
+          // O holds P_{t-1} V_{t-1}: S_t completed, and PV_{t-1} was issued
+          // before it, so it completed too; PV_t waits for P_t.
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t orr[32];
@@ -459,20 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st32(s_addr + 32, pw[1]);
         tc::tmem_st_wait();
         tc::fence_before_sync();
-        // Observe every o_done phase in order, before P_t is published: a parity
-        // wait is only unambiguous while the barrier is at most one phase away,
-        // and PV_t cannot start before P_t exists.
-        if (t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) {
-          ok = false;
-          ++t;
-          break;
-        }
+        // P_t overwrites P_{t-1}, which PV_{t-1} read: done, as it was issued
+        // before S_t, which has completed.
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bar->p_full[x]);
       }
     }
-    // epilogue: O / l and the log-sum-exp of this row (PV_{t-2} observed before P_{t-1})
-    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], (t - 1) & 1))) ok = false;
+    // epilogue: O / l and the log-sum-exp of this row; o_done_x is committed
+    // once, after the last PV_x
+    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done[x], 0))) ok = false;
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     tc::fence_after_sync();
     const int64_t orow = static_cast<int64_t>(part_row + (r0 + row) / G) * a.Hq + kvh * G + (r0 + row) % G;
