@@ -16,7 +16,10 @@
 //              from the paged pool (3-D maps over [tokens, Hkv, d], 128-byte
 //              swizzle, two 64-column halves per tile) into two-stage rings;
 //   warp 9     TMEM allocation and MMA issue (one elected lane);
-//   warps 10-11 idle (they complete the third warpgroup).
+//   warp 10    barrier waits for the MMA warp: it waits on the K/V and P
+//              barriers and hands each ready point to warp 9 through a named
+//              barrier, so the issuing thread never pays an mbarrier wait;
+//   warp 11    idle (it completes the third warpgroup).
 // TMEM (512 columns): S_A | O_A | S_B | O_B, 128 fp32 columns each.
 // Per KV tile j and query tile X:
 //   S_X = Q_X K_j^T      tcgen05.mma kind::f16, M = N = 128, fp32 in TMEM;
@@ -56,7 +59,9 @@ constexpr int kThreads = 384;
 // warpgroups grow to 216 and the producer / MMA warpgroup shrinks to 72:
 // 2 x 128 x 216 + 128 x 72 = 64512 (per SM sub-partition 216 + 216 + 72 <= 512).
 constexpr int kRegsSoftmax = 216, kRegsOther = 72;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kSyncWarp = 10;
+// named barriers between the sync warp and the MMA warp (0 is __syncthreads)
+constexpr int kBarReadyA = 1, kBarReadyB = 2;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
 constexpr uint32_t kTmemCols = 512;
@@ -77,6 +82,7 @@ struct Barriers {
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   uint64_t drain;
   uint32_t tmem_base;
+  uint32_t abort;  // set by the sync warp when a wait timed out
 };
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (2 + 2 * kStages) + sizeof(Barriers);
@@ -181,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bar->o_done[x], 1);
     }
     ptx::mbar_init(&bar->drain, 1);
+    bar->abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -243,32 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(&bar->v_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA
-    // The whole warp walks the tiles and waits on the barriers (a warp-wide
-    // wait is cheaper than one lane's divergent wait); lane 0 issues every
-    // tcgen05.mma and commit.  Commits are kept to three a tile: the tensor
-    // pipe drains while this thread is busy with anything but MMAs.
-    const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
-    const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
-    const int nx = has_b ? 2 : 1;
-    // Descriptors of every operand tile, built once; an MMA only adds an offset.
-    const tc::Desc desc_q0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
-    const tc::Desc desc_k0 = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
-    const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
-    constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
-    // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
-    auto issue_s = [&](int x, int32_t t) {
-      const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
-      const uint32_t d_col = tmem + col_s(x);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-        tc::mma_ss_fast(d_col, desc_q0, qoff + off, desc_k0, koff + off, idesc_qk, kk > 0);
-      }
-      tc::commit(&bar->s_full[x]);
-    };
-    // tile sequence with the valid key count of each tile
+  } else if (warp == kMmaWarp || warp == kSyncWarp) {
+    // The MMA warp and the sync warp walk the same tile sequence.
     int32_t bi = 0, off = 0, n = 0;
     bool have = false;
     auto next_tile = [&](int32_t* nvalid) -> bool {
@@ -293,14 +276,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
     };
-    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
+    const int nx = has_b ? 2 : 1;
+    auto handoff = [&](int id) { asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory"); };
+    auto take = [&](int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); };
+    if (warp == kSyncWarp) {
+      // ------------------------------------------------------------ sync warp
+      // Hands over, in order: Q and K(0) ready; then per tile t: V(t), K(t+1)
+      // and P_A(t) ready (barrier A), P_B(t) ready (barrier B).  Warp 9 takes
+      // each hand-off once, so this warp never runs a hand-off ahead: the next
+      // one needs a P that exists only after warp 9 used the previous one.
+      // On a timeout it flags the abort, hands off once more and stops.
+      bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
+      int32_t nv_cur = 0, nv_next = 0;
+      bool has_cur = ok && next_tile(&nv_cur);
+      if (has_cur) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
+      if (!ok && lane == 0) bar->abort = 1;
+      __syncwarp();
+      handoff(kBarReadyA);
+      int32_t t = 0;
+      while (ok && has_cur) {
+        const bool has_next = next_tile(&nv_next);
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[t % kStages], (t / kStages) & 1));
+        if (ok && has_next)
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[0], t & 1));
+        if (!ok && lane == 0) bar->abort = 1;
+        __syncwarp();
+        handoff(kBarReadyA);
+        if (!ok) break;
+        if (nx == 2) {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[1], t & 1));
+          if (!ok && lane == 0) bar->abort = 1;
+          __syncwarp();
+          handoff(kBarReadyB);
+        }
+        ++t;
+        has_cur = has_next;
+        nv_cur = nv_next;
+      }
+      if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    } else {
+    // ------------------------------------------------------------------ MMA
+    // Lane 0 issues every tcgen05.mma and commit; the warp takes the sync
+    // warp's hand-offs (a named barrier: far cheaper than an mbarrier wait,
+    // and the tensor pipe drains while the issuing thread waits).  Commits
+    // are kept to three a tile.
+    const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
+    const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
+    // Descriptors of every operand tile, built once; an MMA only adds an offset.
+    const tc::Desc desc_q0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc desc_k0 = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
+    constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
+    // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
+    auto issue_s = [&](int x, int32_t t) {
+      const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
+      const uint32_t d_col = tmem + col_s(x);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        tc::mma_ss_fast(d_col, desc_q0, qoff + off, desc_k0, koff + off, idesc_qk, kk > 0);
+      }
+      tc::commit(&bar->s_full[x]);
+    };
+    volatile uint32_t* abort_flag = &bar->abort;
     int32_t nv_cur = 0, nv_next = 0;
-    bool has_cur = ok && next_tile(&nv_cur);
+    bool has_cur = next_tile(&nv_cur);
+    take(kBarReadyA);  // Q, K(0)
+    bool ok = *abort_flag == 0;
     int32_t t = 0;
-    if (has_cur) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
+    if (ok && has_cur) {
       tc::fence_after_sync();
-      if (ok && lane == 0) {
+      if (lane == 0) {
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
         tc::commit(&bar->kv_free[0]);  // release 0: K(0)
       }
@@ -309,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (has_cur && ok) {
       const bool has_next = next_tile(&nv_next);
       const int vs = t % kStages;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[vs], (t / kStages) & 1))) { ok = false; break; }
+      take(kBarReadyA);  // V(t), K(t+1), P_A(t)
+      if (*abort_flag != 0) { ok = false; break; }
       uint8_t* vtile = sv + vs * kTileBytes;
       const int ksteps = (nv_cur + 15) >> 4;
       if (nv_cur < ksteps * 16) {
@@ -323,16 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       const uint32_t voff = vs * kTile16;
-      if (has_next &&
-          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
-        ok = false;
-        break;
-      }
       for (int x = 0; x < nx; ++x) {
         // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[x], t & 1))) {
-          ok = false;
-          break;
+        if (x == 1) {
+          take(kBarReadyB);  // P_B(t)
+          if (*abort_flag != 0) { ok = false; break; }
         }
         tc::fence_after_sync();
         if (lane == 0) {
@@ -367,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    }
   }
   } else {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
