@@ -77,7 +77,9 @@ struct Barriers {
   uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages];
   // kv_free[j % kStages] completes the j-th release: K tile j and V tile j-1
-  // have been consumed by their MMAs (one commit after S(j), issued after PV(j-1))
+  // have been consumed by their MMAs.  S(j) of the last query tile is the last
+  // MMA to read either, so one softmax thread of that tile arrives once it has
+  // seen S(j) complete (MMAs complete in issue order).
   uint64_t kv_free[kStages];
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   uint64_t drain;
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane 0 issues every tcgen05.mma and commit; the warp takes the sync
     // warp's hand-offs (a named barrier: far cheaper than an mbarrier wait,
     // and the tensor pipe drains while the issuing thread waits).  Commits
-    // are kept to three a tile.
+    // are kept to two a tile.
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
     // Descriptors of every operand tile, built once; an MMA only adds an offset.
@@ -349,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       if (lane == 0) {
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
-        tc::commit(&bar->kv_free[0]);  // release 0: K(0)
       }
       __syncwarp();
     }
@@ -396,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(x, t + 1);
           else
             tc::commit(&bar->o_done[x]);
-          if (x == nx - 1) tc::commit(&bar->kv_free[(t + 1) % kStages]);  // release t+1: K(t+1), V(t)
         }
         __syncwarp();
       }
@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + col_s(x), o_addr = lane_addr + col_o(x);
     const bool row_valid = row < n_rows;
+    const bool release_kv = wq == 0 && x == (has_b ? 1 : 0);
     const int32_t my_vis = row_valid ? visible_keys(q_len, kv_len, (r0 + row) / G, a.causal) : 0;
     // every row of this query tile sees the keys below vis_first (uniform over the tile)
     const int32_t vis_first = visible_keys(q_len, kv_len, (r0 + x * kMT) / G, a.causal);
@@ -440,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t nvalid = min(kN, n - off);
         // waits and TMEM accesses stay warp-uniform (tcgen05.ld/st are warp-collective)
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1))) { ok = false; break; }
+        if (release_kv && lane == 0) ptx::mbar_arrive(&bar->kv_free[t % kStages]);  // release t
         tc::fence_after_sync();
         uint32_t sr[4][32];
 #pragma unroll
