@@ -319,7 +319,7 @@ def run_ours(args, dctx):
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
-    roof.update({"traffic": traffic_for(kname, w.name), "kernel": f"partial_{kname}",
+    roof.update({"traffic": traffic_for(f"partial_{kname}", w.name), "kernel": f"partial_{kname}",
                  "kernel_ms": partial_ms, "merge_ms": merge_ms, "peak_source": peak_src,
                  "algorithmic_per_launch": acc["partial_bytes"] if hbm_bound else acc["flops"]})
 
