@@ -369,12 +369,20 @@ def run_backward(args, dctx, w, inp, run, out, lse, acc):
     s = t0.elapsed_time(t1) / 1e3 / args.steps
     flops = 2.5 * acc["flops"]
     peaks, src = load_peaks()
+    tc = run.kernel_used() == K.KERNEL_TC
+    kname = "backward_tcgen05" if tc else "backward_simt"
+    if tc:
+        roof = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": flops / s / 1e12 / peaks["bf16_tflops"], "peak_source": src,
+                "note": "dQ and dK/dV tensor-core kernels plus delta and dQ reduction, whole backward step"}
+    else:
+        roof = {"bound": "fp32_fma", "achieved": flops / s / 1e12, "unit": "TFLOP/s",
+                "note": "CUDA-core kernel: bf16 inputs, fp32 FMA arithmetic"}
     line = {"metric": METRIC + " (backward pass)", "value": flops / s / 1e12, "unit": "TFLOP/s",
             "n_gpus": dctx.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s,
             "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "shape": w.description, "kernel": "backward_simt"},
-            "roofline": {"bound": "fp32_fma", "achieved": flops / s / 1e12, "unit": "TFLOP/s",
-                         "note": "CUDA-core kernel: bf16 inputs, fp32 FMA arithmetic"}}
+            "config": {"workload": w.name, "shape": w.description, "kernel": kname},
+            "roofline": roof}
     if dctx.rank == 0:
         print(json.dumps(line), flush=True)
     dctx.finish()

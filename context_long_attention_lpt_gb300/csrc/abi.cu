@@ -250,7 +250,14 @@ extern "C" int splitkv_attn_backward(const void* q, const void* k_pool, const vo
   if (n_items > 0 && (!dout || !lse || !delta || !dk_pool || !dv_pool))
     return fail(SPLITKV_ERR_INVALID, "null device pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the partial dQ rows collect atomic adds from every key tile of their item
+  if (n_items > 0 && splitkv::bwd_tc_supports(a)) {
+    // tensor cores: every partial dQ row and every key's dK / dV written once
+    st = splitkv::launch_bwd_tc(a, dout, lse, delta, dq_part, dk_pool, dv_pool, s);
+    if (st != SPLITKV_OK) return st;
+    splitkv::clear_error();
+    return SPLITKV_OK;
+  }
+  // CUDA cores: the partial dQ rows collect atomic adds from every key tile of their item
   cudaError_t e = cudaMemsetAsync(dq_part, 0, static_cast<size_t>(part_rows) * Hq * d * sizeof(float), s);
   if (e == cudaSuccess && n_items > 0) e = splitkv::launch_bwd_partial(a, dout, lse, delta, dq_part, dk_pool, dv_pool, s);
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));

@@ -1,0 +1,745 @@
+// Tensor-core backward of the split-KV attention for sm_103a: TMA + tcgen05 +
+// TMEM.  Same results as the CUDA-core backward in backward.cu (per-shard dK,
+// dV and partial dQ over the work items), for the shapes the forward's
+// tensor-core kernel takes: bf16, d = 128, block_len % 128 == 0, G | 128.
+//
+// The Split-KV card places the method in training (card intro) and states it
+// is exact ("All Facts").  With the merged forward's L and D = rowsum(dO * O),
+// a shard's keys need only query-sized tensors:
+//   P = exp(s - L), dP = dO V^T, dS = P (dP - D),
+//   dQ_i = scale dS K   (partial, summed over the shards by splitkv_dq_reduce),
+//   dK = scale dS^T Q,  dV = P^T dO.
+//
+// Two kernels:
+//  * bwd_dq_tc_kernel: one CTA per (work item, K/V head, 128 query rows).  It
+//    walks the item's key tiles like the forward: S = Q K^T and dP = dO V^T in
+//    TMEM, the row threads form dS (bf16) over S, then dQ += dS K.
+//  * bwd_dkdv_tc_kernel: one CTA per (work item, K/V head, a stride of the
+//    item's 128-key tiles).  Keys sit in the TMEM lanes: S^T = K Q^T and
+//    dP^T = V dO^T, the key threads form P^T and dS^T (bf16) in place, then
+//    dV += P^T dO and dK += dS^T Q accumulate over all query rows of the
+//    sequence, 128 at a time.
+// Every wait has a time limit; on expiry the status word gets bit 2 and the
+// CTA unwinds (all MMAs drained, TMEM freed).
+
+#include <cmath>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+#include "status.h"
+#include "tc_ptx.cuh"
+#include "tensor_map.h"
+
+namespace splitkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kRows = 128;  // query rows per tile
+constexpr int kN = 128;     // keys per tile
+constexpr int kStages = 2;
+constexpr uint32_t kHalfBytes = 128 * 64 * 2;    // 128 rows x 64 bf16: one swizzled half
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile
+constexpr uint32_t kTile16 = kTileBytes >> 4;    // in descriptor address units
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 192;  // warps 0-3: elementwise (one TMEM lane each); 4: TMA; 5: MMA
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+
+// TMEM columns (both kernels): scores, dP, then one or two fp32 accumulators.
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
+
+// Byte offset (>> 4) of 16-wide K step kk inside a K-major SW128 tile made of two
+// 64-column halves: steps 0-3 in the first half, 4-7 in the second.
+__device__ __forceinline__ uint32_t kstep_off(int kk) { return ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4; }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// One item's key blocks: keys [lo, lo + n) of block bi that some row of the
+// unit can see, or -1 (nothing to read; *bad if the block-table entry is out
+// of the pool).
+struct ItemBlocks {
+  const int32_t* blocks;
+  const int32_t* table;
+  int32_t blk_cnt, bl, max_blocks, kv_len, vis_max;
+  int64_t n_pool;
+  __device__ __forceinline__ int32_t block(int32_t bi, int32_t* lo, int32_t* n, bool* bad) const {
+    const int32_t j = __ldg(blocks + bi);
+    *lo = j * bl;
+    *n = min(min(bl, kv_len - *lo), vis_max - *lo);
+    *bad = false;
+    if (*n <= 0) return -1;
+    const int32_t phys = j < max_blocks ? __ldg(table + j) : -1;
+    if (phys < 0 || phys >= n_pool) {
+      *bad = true;
+      return -1;
+    }
+    return phys;
+  }
+};
+
+// Tiles of the item in order, for the roles that only need their key counts.
+struct TileSeq {
+  ItemBlocks ib;
+  int32_t bi = 0, off = 0, n = 0, lo = 0, phys = -1;
+  bool have = false;
+  bool bad_seen = false;  // a block-table entry outside the pool was skipped
+  __device__ __forceinline__ bool next(int32_t* pos0, int32_t* nvalid, int32_t* tok) {
+    while (true) {
+      if (have && off + kN < n) {
+        off += kN;
+        break;
+      }
+      have = false;
+      while (bi < ib.blk_cnt && !have) {
+        bool bad;
+        phys = ib.block(bi++, &lo, &n, &bad);
+        bad_seen |= bad;
+        if (phys >= 0) {
+          have = true;
+          off = 0;
+        }
+      }
+      if (!have) return false;
+      break;
+    }
+    *pos0 = lo + off;
+    *nvalid = min(kN, n - off);
+    *tok = phys * ib.bl + off;
+    return true;
+  }
+};
+
+// ============================================================== dQ kernel
+
+struct DqBarriers {
+  uint64_t qd_full;                  // Q and dO tiles of the unit
+  uint64_t kv_full[kStages];         // K(t) and V(t)
+  uint64_t kv_free[kStages];         // the slot's dQ MMA has read K(t)
+  uint64_t s_full, ds_full, o_done, drain;
+  uint32_t tmem_base;
+};
+constexpr size_t kDqSmem = 1024 + kTileBytes * (2 + 2 * kStages) + sizeof(DqBarriers);
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
+                     float* __restrict__ dq_part, int32_t units_per_item, const __grid_constant__ CUtensorMap tmap_q,
+                     const __grid_constant__ CUtensorMap tmap_do, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;                       // Q tile
+  uint8_t* sdo = smem + kTileBytes;         // dO tile
+  uint8_t* sk = smem + 2 * kTileBytes;      // K ring
+  uint8_t* sv = sk + kStages * kTileBytes;  // V ring
+  DqBarriers* bar = reinterpret_cast<DqBarriers*>(sv + kStages * kTileBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = blockIdx.x;
+  const int32_t utile = static_cast<int32_t>(u % units_per_item);
+  const int32_t kvh = static_cast<int32_t>((u / units_per_item) % a.Hkv);
+  const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(units_per_item) * a.Hkv));
+
+  const WorkView wv(a.work);
+  const int32_t* it = wv.item(item);
+  const int32_t seq = __ldg(it + kItSeq);
+  const int32_t part_row = __ldg(it + kItPartRow);
+  const int32_t* sqrow = wv.seq(seq);
+  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t G = a.Hq / a.Hkv;
+  const int32_t rows = q_len * G;
+  const int32_t r0 = utile * kRows;
+  if (r0 >= rows) return;  // uniform over the CTA
+  if (part_row < 0 || static_cast<int64_t>(part_row) + q_len > a.part_rows) {
+    if (threadIdx.x == 0) atomicOr(a.status, 2u);
+    return;
+  }
+  const int32_t n_rows = min(kRows, rows - r0);
+  const int32_t vis_last = visible_keys(q_len, kv_len, (r0 + n_rows - 1) / G, a.causal);
+  TileSeq tiles;
+  tiles.ib = ItemBlocks{wv.blocks() + __ldg(it + kItBlockOff),
+                        a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq, __ldg(it + kItBlockCnt),
+                        a.block_len, a.max_blocks_per_seq, kv_len, vis_last, a.n_pool_blocks};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar->qd_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&bar->kv_full[s], 1);
+      ptx::mbar_init(&bar->kv_free[s], 1);
+    }
+    ptx::mbar_init(&bar->s_full, 1);
+    ptx::mbar_init(&bar->ds_full, 4);
+    ptx::mbar_init(&bar->o_done, 1);
+    ptx::mbar_init(&bar->drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(&bar->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bar->tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_q);
+      ptx::prefetch_tmap(&tmap_do);
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+      const int32_t tok0 = cu_q + r0 / G;
+      ptx::mbar_arrive_expect_tx(&bar->qd_full, 2 * kTileBytes);
+      ptx::tma_load_3d(sq, &tmap_q, 0, kvh * G, tok0, &bar->qd_full);
+      ptx::tma_load_3d(sq + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->qd_full);
+      ptx::tma_load_3d(sdo, &tmap_do, 0, kvh * G, tok0, &bar->qd_full);
+      ptx::tma_load_3d(sdo + kHalfBytes, &tmap_do, 64, kvh * G, tok0, &bar->qd_full);
+      int32_t t = 0, pos0, nv, tok;
+      bool ok = true;
+      while (ok && tiles.next(&pos0, &nv, &tok)) {
+        const int s = t % kStages;
+        if (t >= kStages && !ptx::mbar_wait(&bar->kv_free[s], ((t - kStages) / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
+        ptx::tma_load_3d(sk + s * kTileBytes, &tmap_k, 0, kvh, tok, &bar->kv_full[s]);
+        ptx::tma_load_3d(sk + s * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->kv_full[s]);
+        ptx::tma_load_3d(sv + s * kTileBytes, &tmap_v, 0, kvh, tok, &bar->kv_full[s]);
+        ptx::tma_load_3d(sv + s * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->kv_full[s]);
+        ++t;
+      }
+      if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
+      // every copy issued has landed before shared memory is released
+      if (!ptx::mbar_wait(&bar->qd_full, 0)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, t - kStages); v < t; ++v)
+        if (!ptx::mbar_wait(&bar->kv_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    // Per tile t: S(t) = Q K(t)^T and dP(t) = dO V(t)^T; once the row threads
+    // have put dS(t) over S(t): dQ += dS(t) K(t).  S(t+1) is issued after
+    // dQ(t), which read dS(t) from the same columns (MMAs run in order).
+    const uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kN, false, false);
+    const uint32_t idesc_dq = tc::idesc_bf16_f32(kRows, kD, false, true);
+    const tc::Desc dq0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc ddo = tc::split(tc::smem_desc(ptx::smem_addr(sdo), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dk = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dv = tc::split(tc::smem_desc(ptx::smem_addr(sv), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dk_mn = tc::split(tc::smem_desc(ptx::smem_addr(sk), kHalfBytes, 1024, tc::kSwizzle128B));
+    auto issue_s_dp = [&](int32_t t) {
+      const uint32_t soff = (t % kStages) * kTile16;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_ss_fast(tmem + kColS, dq0, kstep_off(kk), dk, soff + kstep_off(kk), idesc_s, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_ss_fast(tmem + kColDP, ddo, kstep_off(kk), dv, soff + kstep_off(kk), idesc_s, kk > 0);
+      tc::commit(&bar->s_full);
+    };
+    TileSeq walk = tiles;
+    int32_t pos0, nv_cur = 0, nv_next = 0, tok;
+    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full, 0));
+    bool has_cur = ok && walk.next(&pos0, &nv_cur, &tok);
+    int32_t t = 0;
+    if (has_cur) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full[0], 0));
+      tc::fence_after_sync();
+      if (ok && lane == 0) issue_s_dp(0);
+      __syncwarp();
+    }
+    while (has_cur && ok) {
+      const bool has_next = walk.next(&pos0, &nv_next, &tok);
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full, t & 1))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int s = t % kStages;
+      const int ksteps = (nv_cur + 15) >> 4;
+      if (nv_cur < ksteps * 16) {
+        // K rows of keys past the end inside the last 16-key step: zero (their dS
+        // is 0, but the pool slot may hold anything); S(t) has read them already
+        uint8_t* ktile = sk + s * kTileBytes;
+        for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
+          const int cc = lane & 15;
+          reinterpret_cast<uint4*>(ktile + (cc < 8 ? 0 : kHalfBytes) + r * 128)[cc & 7] = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        for (int kk = 0; kk < ksteps; ++kk)
+          tc::mma_ts_fast(tmem + kColAcc0, tmem + kColS + 8 * kk, dk_mn, s * kTile16 + kk * (2048 >> 4), idesc_dq,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bar->kv_free[s]);
+        if (!has_next) tc::commit(&bar->o_done);
+      }
+      __syncwarp();
+      if (has_next) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) issue_s_dp(t + 1);
+        __syncwarp();
+      }
+      ++t;
+      has_cur = has_next;
+      nv_cur = nv_next;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    if (lane == 0) tc::commit(&bar->drain);
+    __syncwarp();
+    if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+  } else {
+    // ----------------------------------------------------- row threads (dS)
+    const int32_t row = warp * 32 + lane;  // TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool row_valid = row < n_rows;
+    const int32_t token = (r0 + row) / G, h = kvh * G + (r0 + row) % G;
+    const int64_t grow = static_cast<int64_t>(cu_q + token) * a.Hq + h;
+    const float L = row_valid ? __ldg(lse + grow) : -INFINITY;
+    const float Dr = row_valid ? __ldg(delta + grow) : 0.f;
+    const bool live = L != -INFINITY;  // a row with no visible key has no gradient
+    const float c = a.scale * kLog2e, lc = live ? L * kLog2e : 0.f;
+    const int32_t my_vis = row_valid ? visible_keys(q_len, kv_len, token, a.causal) : 0;
+    TileSeq walk = tiles;
+    int32_t pos0, nvalid, tok, t = 0;
+    bool ok = true;
+    while (ok && walk.next(&pos0, &nvalid, &tok)) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full, t & 1))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int32_t lim = live ? min(nvalid, my_vis - pos0) : 0;  // keys [0, lim) of the tile are seen
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[2][32], dp[2][32], pk[32];
+        tc::tmem_ld32(lane_addr + kColS + 64 * hh, sr[0]);
+        tc::tmem_ld32(lane_addr + kColS + 64 * hh + 32, sr[1]);
+        tc::tmem_ld32(lane_addr + kColDP + 64 * hh, dp[0]);
+        tc::tmem_ld32(lane_addr + kColDP + 64 * hh + 32, dp[1]);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int j = 64 * hh + 32 * q + i;
+            float ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float p = fast_exp2(__uint_as_float(sr[q][i + e]) * c - lc);
+              ds[e] = j + e < lim ? p * (__uint_as_float(dp[q][i + e]) - Dr) : 0.f;
+            }
+            pk[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+          }
+        // dS as bf16 over S columns [32 hh, 32 hh + 32): all already read
+        tc::tmem_st32(lane_addr + kColS + 32 * hh, pk);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bar->ds_full);
+      ++t;
+    }
+    // epilogue: dQ = scale * sum dS K
+    if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, 0))) ok = false;
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    tc::fence_after_sync();
+    const int64_t orow = static_cast<int64_t>(part_row + token) * a.Hq + h;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t acc[32];
+      if (t > 0) {
+        tc::tmem_ld32(lane_addr + kColAcc0 + 32 * q4, acc);
+        tc::tmem_ld_wait();
+      }
+      if (row_valid) {
+        float4* dst = reinterpret_cast<float4*>(dq_part + orow * kD + 32 * q4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (t > 0)
+            v = make_float4(__uint_as_float(acc[4 * i]) * a.scale, __uint_as_float(acc[4 * i + 1]) * a.scale,
+                            __uint_as_float(acc[4 * i + 2]) * a.scale, __uint_as_float(acc[4 * i + 3]) * a.scale);
+          dst[i] = v;
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ========================================================== dK / dV kernel
+
+constexpr int kKeySplit = 16;  // CTAs per (item, K/V head); each takes every 16th key tile
+
+struct KvBarriers {
+  uint64_t kv_full;              // K and V of the current key tile
+  uint64_t qd_full[kStages];     // Q, dO (TMA) and L, D (producer lanes) of a row tile
+  uint64_t qd_free[kStages];     // the row tile's dV / dK MMAs have read Q and dO
+  uint64_t s_full, ds_full;      // S^T, dP^T in TMEM; P^T, dS^T written back
+  uint64_t o_done;               // the key tile's last dV / dK MMA completed
+  uint64_t drain;
+  uint32_t tmem_base;
+  float ld[kStages][2][kRows];   // L and D of the row tile's rows
+};
+constexpr size_t kKvSmem = 1024 + kTileBytes * (2 + 2 * kStages) + sizeof(KvBarriers);
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
+                       float* __restrict__ dk_pool, float* __restrict__ dv_pool,
+                       const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
+                       const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sk = smem;                        // K tile
+  uint8_t* sv = smem + kTileBytes;           // V tile
+  uint8_t* sq = smem + 2 * kTileBytes;       // Q ring
+  uint8_t* sdo = sq + kStages * kTileBytes;  // dO ring
+  KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kStages * kTileBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t split = static_cast<int32_t>(blockIdx.x % kKeySplit);
+  const int32_t kvh = static_cast<int32_t>((blockIdx.x / kKeySplit) % a.Hkv);
+  const int32_t item = static_cast<int32_t>(blockIdx.x / (kKeySplit * a.Hkv));
+
+  const WorkView wv(a.work);
+  const int32_t* it = wv.item(item);
+  const int32_t seq = __ldg(it + kItSeq);
+  const int32_t* sqrow = wv.seq(seq);
+  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t G = a.Hq / a.Hkv;
+  const int32_t rows = q_len * G;
+  const int32_t n_rt = (rows + kRows - 1) / kRows;  // row tiles of the sequence
+  // every key below kv_len gets a gradient (zero if no row sees it)
+  TileSeq tiles;
+  tiles.ib = ItemBlocks{wv.blocks() + __ldg(it + kItBlockOff),
+                        a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq, __ldg(it + kItBlockCnt),
+                        a.block_len, a.max_blocks_per_seq, kv_len, kv_len, a.n_pool_blocks};
+  // this CTA's key tiles: ordinals split, split + kKeySplit, ... of the item's tiles
+  auto next_mine = [&](TileSeq& w, int32_t& ord, int32_t* pos0, int32_t* nv, int32_t* tok) -> bool {
+    while (w.next(pos0, nv, tok)) {
+      if (ord++ % kKeySplit == split) return true;
+    }
+    return false;
+  };
+  if (n_rt == 0) return;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&bar->qd_full[s], 1);
+      ptx::mbar_init(&bar->qd_free[s], 1);
+    }
+    ptx::mbar_init(&bar->s_full, 1);
+    ptx::mbar_init(&bar->ds_full, 4);
+    ptx::mbar_init(&bar->o_done, 1);
+    ptx::mbar_init(&bar->drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(&bar->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bar->tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------- producer
+    // Per key tile: K and V (after the previous key tile's MMAs are done),
+    // then every row tile's Q, dO by TMA and L, D by the warp's lanes.
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_q);
+      ptx::prefetch_tmap(&tmap_do);
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+    }
+    TileSeq walk = tiles;
+    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
+    bool ok = true;
+    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
+      if (kt > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (kt - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&bar->kv_full, 2 * kTileBytes);
+        ptx::tma_load_3d(sk, &tmap_k, 0, kvh, tok, &bar->kv_full);
+        ptx::tma_load_3d(sk + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->kv_full);
+        ptx::tma_load_3d(sv, &tmap_v, 0, kvh, tok, &bar->kv_full);
+        ptx::tma_load_3d(sv + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->kv_full);
+      }
+      for (int32_t r = 0; r < n_rt; ++r, ++rt) {
+        const int s = rt % kStages;
+        if (rt >= kStages && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_free[s], ((rt - kStages) / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        // L and D of rows r*128 .. r*128+127 (rows past the sequence: L = -inf)
+        for (int i = lane; i < kRows; i += 32) {
+          const int32_t row = r * kRows + i;
+          float L = -INFINITY, Dv = 0.f;
+          if (row < rows) {
+            const int64_t g = static_cast<int64_t>(cu_q + row / G) * a.Hq + kvh * G + row % G;
+            L = __ldg(lse + g);
+            Dv = __ldg(delta + g);
+          }
+          bar->ld[s][0][i] = L;
+          bar->ld[s][1][i] = Dv;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t tok0 = cu_q + (r * kRows) / G;
+          ptx::mbar_arrive_expect_tx(&bar->qd_full[s], 2 * kTileBytes);
+          ptx::tma_load_3d(sq + s * kTileBytes, &tmap_q, 0, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sq + s * kTileBytes + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sdo + s * kTileBytes, &tmap_do, 0, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sdo + s * kTileBytes + kHalfBytes, &tmap_do, 64, kvh * G, tok0, &bar->qd_full[s]);
+        }
+      }
+      ++kt;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    if (walk.bad_seen && lane == 0) atomicOr(a.status, 1u);
+    // every copy issued has landed before shared memory is released
+    if (lane == 0) {
+      if (kt > 0 && !ptx::mbar_wait(&bar->kv_full, (kt - 1) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, rt - kStages); v < rt; ++v)
+        if (!ptx::mbar_wait(&bar->qd_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    // Per row tile: S^T = K Q^T, dP^T = V dO^T; once the key threads have put
+    // P^T and dS^T over them: dV += P^T dO, dK += dS^T Q.  The next row tile's
+    // S^T is issued after those, which read the same columns (MMAs run in order).
+    const uint32_t idesc_s = tc::idesc_bf16_f32(kN, kRows, false, false);
+    const uint32_t idesc_acc = tc::idesc_bf16_f32(kN, kD, false, true);
+    const tc::Desc dk = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dv = tc::split(tc::smem_desc(ptx::smem_addr(sv), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dq = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc ddo = tc::split(tc::smem_desc(ptx::smem_addr(sdo), 16, 1024, tc::kSwizzle128B));
+    const tc::Desc dq_mn = tc::split(tc::smem_desc(ptx::smem_addr(sq), kHalfBytes, 1024, tc::kSwizzle128B));
+    const tc::Desc ddo_mn = tc::split(tc::smem_desc(ptx::smem_addr(sdo), kHalfBytes, 1024, tc::kSwizzle128B));
+    TileSeq walk = tiles;
+    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
+    bool ok = true;
+    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full, kt & 1))) {
+        ok = false;
+        break;
+      }
+      for (int32_t r = 0; r < n_rt; ++r, ++rt) {
+        const int s = rt % kStages;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qoff = s * kTile16;
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc::mma_ss_fast(tmem + kColS, dk, kstep_off(kk), dq, qoff + kstep_off(kk), idesc_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc::mma_ss_fast(tmem + kColDP, dv, kstep_off(kk), ddo, qoff + kstep_off(kk), idesc_s, kk > 0);
+          tc::commit(&bar->s_full);
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full, rt & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColS + 8 * kk, ddo_mn, qoff + kk * (2048 >> 4), idesc_acc,
+                            (r > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDP + 8 * kk, dq_mn, qoff + kk * (2048 >> 4), idesc_acc,
+                            (r > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&bar->qd_free[s]);
+          if (r == n_rt - 1) tc::commit(&bar->o_done);
+        }
+        __syncwarp();
+      }
+      ++kt;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+    if (lane == 0) tc::commit(&bar->drain);
+    __syncwarp();
+    if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+  } else {
+    // ------------------------------------------------ key threads (P^T, dS^T)
+    const int32_t k = warp * 32 + lane;  // TMEM lane = key of the tile
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = a.scale * kLog2e;
+    TileSeq walk = tiles;
+    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
+    bool ok = true;
+    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
+      const bool key_valid = k < nv;
+      // causal: the row (token t, head) sees this key iff t >= pos - (kv_len - q_len)
+      const int32_t t_first = a.causal ? max(0, pos0 + k - (kv_len - q_len)) : 0;
+      for (int32_t r = 0; r < n_rt; ++r, ++rt) {
+        const int s = rt % kStages;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kStages) & 1)) ||
+            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full, rt & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        // rows j of the tile this key contributes to: [jmin, jmax)
+        const int32_t jmin = key_valid ? max(0, t_first * G - r * kRows) : kRows;
+        const int32_t jmax = min(kRows, rows - r * kRows);
+        const float* Ls = bar->ld[s][0];
+        const float* Ds = bar->ld[s][1];
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[2][32], dp[2][32], pk[32], dk2[32];
+          tc::tmem_ld32(lane_addr + kColS + 64 * hh, sr[0]);
+          tc::tmem_ld32(lane_addr + kColS + 64 * hh + 32, sr[1]);
+          tc::tmem_ld32(lane_addr + kColDP + 64 * hh, dp[0]);
+          tc::tmem_ld32(lane_addr + kColDP + 64 * hh + 32, dp[1]);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float p[2], ds[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int j = 64 * hh + 32 * q + i + e;
+                const float Lj = Ls[j];
+                const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
+                const float pj = fast_exp2(__uint_as_float(sr[q][i + e]) * c - Lj * kLog2e);
+                p[e] = on ? pj : 0.f;
+                ds[e] = on ? pj * (__uint_as_float(dp[q][i + e]) - Ds[j]) : 0.f;
+              }
+              pk[16 * q + i / 2] = pack_bf16(p[0], p[1]);
+              dk2[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+            }
+          // P^T over S^T columns, dS^T over dP^T columns [32 hh, 32 hh + 32): all already read
+          tc::tmem_st32(lane_addr + kColS + 32 * hh, pk);
+          tc::tmem_st32(lane_addr + kColDP + 32 * hh, dk2);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bar->ds_full);
+      }
+      if (!ok) break;
+      // epilogue: this key's dV and dK = scale * sum dS^T Q
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, kt & 1))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int64_t krow = (static_cast<int64_t>(tok) + k) * a.Hkv + kvh;  // pool token tok + k
+#pragma unroll 1
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const bool is_k = q4 >= 4;
+        uint32_t acc[32];
+        tc::tmem_ld32(lane_addr + (is_k ? kColAcc1 : kColAcc0) + 32 * (q4 & 3), acc);
+        tc::tmem_ld_wait();
+        if (key_valid) {
+          const float f = is_k ? a.scale : 1.f;
+          float4* dst = reinterpret_cast<float4*>((is_k ? dk_pool : dv_pool) + krow * kD + 32 * (q4 & 3));
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(acc[4 * i]) * f, __uint_as_float(acc[4 * i + 1]) * f,
+                                 __uint_as_float(acc[4 * i + 2]) * f, __uint_as_float(acc[4 * i + 3]) * f);
+        }
+      }
+      ++kt;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int make_maps(const PartialArgs& a, const void* dout, CUtensorMap* tq, CUtensorMap* tdo, CUtensorMap* tk,
+              CUtensorMap* tv) {
+  const int32_t G = a.Hq / a.Hkv;
+  const uint64_t qdims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
+  const uint64_t qstrides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hq) * kD * 2ull};
+  const uint32_t qbox[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kRows / G)};
+  int st = encode_bf16_3d(tq, a.q, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == SPLITKV_OK) st = encode_bf16_3d(tdo, dout, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t kdims[3] = {kD, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.n_pool_blocks) * a.block_len};
+  const uint64_t kstrides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hkv) * kD * 2ull};
+  const uint32_t kbox[3] = {64, 1, kN};
+  if (st == SPLITKV_OK) st = encode_bf16_3d(tk, a.k_pool, kdims, kstrides, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == SPLITKV_OK) st = encode_bf16_3d(tv, a.v_pool, kdims, kstrides, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  return st;
+}
+
+}  // namespace
+
+bool bwd_tc_supports(const PartialArgs& a) {
+  if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
+  const int32_t G = a.Hq / a.Hkv;
+  return G >= 1 && G <= kRows && kRows % G == 0 && a.block_len % kN == 0 &&
+         static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
+}
+
+int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, const float* delta, float* dq_part,
+                  float* dk_pool, float* dv_pool, cudaStream_t stream) {
+  const int32_t G = a.Hq / a.Hkv;
+  const int32_t units = (a.max_q_len * G + kRows - 1) / kRows;
+  const int64_t grid = static_cast<int64_t>(units) * a.Hkv * a.n_items;
+  if (grid == 0) return SPLITKV_OK;
+  if (grid > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many backward units");
+  CUtensorMap tq, tdo, tk, tv;
+  int st = make_maps(a, dout, &tq, &tdo, &tk, &tv);
+  if (st != SPLITKV_OK) return st;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDqSmem));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward smem attribute: %s", cudaGetErrorString(e));
+  bwd_dq_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kDqSmem, stream>>>(a, lse, delta, dq_part, units, tq, tdo,
+                                                                                 tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dQ launch: %s", cudaGetErrorString(e));
+  const int64_t grid_kv = static_cast<int64_t>(kKeySplit) * a.Hkv * a.n_items;
+  if (grid_kv > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many backward units");
+  e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKvSmem));
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward smem attribute: %s", cudaGetErrorString(e));
+  bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kThreads, kKvSmem, stream>>>(a, lse, delta, dk_pool, dv_pool,
+                                                                                     tq, tdo, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dK/dV launch: %s", cudaGetErrorString(e));
+  return SPLITKV_OK;
+}
+
+}  // namespace splitkv

@@ -55,6 +55,10 @@ bool tc_supports(const PartialArgs& a);
 // Backward pass (backward.cu).
 cudaError_t launch_bwd_delta(const void* o, const void* dout, int64_t n_rows, int32_t d, int32_t dtype, float* delta,
                              cudaStream_t stream);
+// Tensor-core backward (bf16, d = 128, block_len % 128 == 0, G | 128).
+bool bwd_tc_supports(const PartialArgs& a);
+int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, const float* delta, float* dq_part,
+                  float* dk_pool, float* dv_pool, cudaStream_t stream);
 cudaError_t launch_bwd_partial(const PartialArgs& a, const void* dout, const float* lse, const float* delta,
                                float* dq_part, float* dk_pool, float* dv_pool, cudaStream_t stream);
 cudaError_t launch_dq_reduce(const float* dq_part, int64_t part_rows, const int32_t* work, int32_t B, int32_t total_q,

@@ -241,14 +241,18 @@ int splitkv_attention_noalloc(const void* q, const void* k_pool, const void* v_p
 int splitkv_bwd_delta(const void* o, const void* dout, int32_t total_q, int32_t Hq, int32_t d,
                       int32_t dtype, float* delta, void* stream);
 
-/* Per-shard backward over the work items of splitkv_build_work (CUDA cores).
+/* Per-shard backward over the work items of splitkv_build_work.  Tensor cores
+ * (tcgen05) for bf16, d = 128, block_len % 128 == 0 and Hq/Hkv dividing 128;
+ * CUDA cores otherwise.
  * In (device): q, k_pool, v_pool, block_table, work as for the forward; dout
  * [total_q, Hq, d] (dtype); lse fp32 [total_q, Hq] (splitkv_merge's lse_out);
  * delta fp32 [total_q, Hq].  Out (device, fp32): dq_part [part_rows, Hq, d]
- * (item i's partial dQ in its part_row slab; zeroed and accumulated by this
- * call), dk_pool / dv_pool [n_pool_blocks, block_len, Hkv, d]: the gradient of
+ * (item i's partial dQ in its part_row slab; every row written by this call),
+ * dk_pool / dv_pool [n_pool_blocks, block_len, Hkv, d]: the gradient of
  * every key position < kv_len of every sequence is written; other positions
- * are left untouched. */
+ * are left untouched.  The pages give the backward no formula; this is the
+ * chain rule through the forward with the merged L saved (card intro:
+ * training with short queries and long contexts). */
 int splitkv_attn_backward(const void* q, const void* k_pool, const void* v_pool, int64_t n_pool_blocks,
                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* work,
                           int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,

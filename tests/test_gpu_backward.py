@@ -1,8 +1,10 @@
-"""GPU parity of the split-KV backward pass (CUDA cores) against the fp64 oracle.
+"""GPU parity of the split-KV backward pass against the fp64 oracle.
 
 The CUDA path computes per-shard dK / dV and partial dQ over the LPT plan's work
 items, then sums the partial dQ; the oracle differentiates the unsharded
-attention.  Gradients are compared element by element."""
+attention.  Gradients are compared element by element.  The bf16 d=128 cases run
+the tensor-core kernels (bf16 P and dS feed the MMAs); fp32 and d=64 the CUDA-core
+kernel."""
 
 import pytest
 import torch
