@@ -369,7 +369,8 @@ def run_backward(args, dctx, w, inp, run, out, lse, acc):
     s = t0.elapsed_time(t1) / 1e3 / args.steps
     flops = 2.5 * acc["flops"]
     peaks, src = load_peaks()
-    tc = run.kernel_used() == K.KERNEL_TC
+    code = K.SPLITKV_BF16 if w.dtype == "bf16" else K.SPLITKV_F32
+    tc = K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, code) == K.KERNEL_TC
     kname = "backward_tcgen05" if tc else "backward_simt"
     if tc:
         roof = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",

@@ -53,6 +53,17 @@ extern "C" int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t b
   return pick_kernel(a, SPLITKV_KERNEL_AUTO);
 }
 
+extern "C" int splitkv_backward_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t dtype) {
+  splitkv::PartialArgs a{};
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.block_len = block_len;
+  a.dtype = dtype;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return fail(SPLITKV_ERR_INVALID, "bad head counts");
+  return splitkv::bwd_tc_supports(a) ? SPLITKV_KERNEL_TC : SPLITKV_KERNEL_SIMT;
+}
+
 namespace {
 
 // Validates the arguments shared by the partial-attention entry points and fills `a`.

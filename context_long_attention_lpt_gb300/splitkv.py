@@ -32,6 +32,7 @@ _SIGNATURES = {
     "splitkv_work_words": (_i64, [_i64, _i32]),
     "splitkv_build_work": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _p, _i64, _p, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "splitkv_backward_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32]),
     "splitkv_attn_partial": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32,
                                              _i32, _i32, _i32, _i32, _f32, _i32, _i32, _p, _p, _i64,
                                              _i32, _p]),
@@ -162,6 +163,10 @@ def splitkv_build_work(q_len, kv_len, block_len, block_cost, shard_of_block, n_s
 
 def splitkv_auto_kernel(Hq, Hkv, d, block_len, max_q_len, dtype):
     return _check("splitkv_auto_kernel", lib().splitkv_auto_kernel(Hq, Hkv, d, block_len, max_q_len, dtype))
+
+
+def splitkv_backward_kernel(Hq, Hkv, d, block_len, dtype):
+    return _check("splitkv_backward_kernel", lib().splitkv_backward_kernel(Hq, Hkv, d, block_len, dtype))
 
 
 # ---------------------------------------------------------------- device calls

@@ -253,6 +253,10 @@ int splitkv_bwd_delta(const void* o, const void* dout, int32_t total_q, int32_t 
  * are left untouched.  The pages give the backward no formula; this is the
  * chain rule through the forward with the merged L saved (card intro:
  * training with short queries and long contexts). */
+/* Which kernel splitkv_attn_backward runs for a shape: SPLITKV_KERNEL_TC or
+ * SPLITKV_KERNEL_SIMT (a negative status for bad head counts). */
+int splitkv_backward_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t dtype);
+
 int splitkv_attn_backward(const void* q, const void* k_pool, const void* v_pool, int64_t n_pool_blocks,
                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* work,
                           int32_t n_items, int32_t B, int32_t total_q, int32_t max_q_len, int32_t Hq,

@@ -167,6 +167,10 @@ def test_errors_are_statuses_not_crashes(k):
                                   1.0, 0, 1, None, None, 0, 0, None) == -2
     assert L.splitkv_merge(None, None, 0, None, 1, 4, 4, 128, 5, None, None, None) == -1
     assert L.splitkv_auto_kernel(4, 3, 128, 128, 1, 1) < 0
+    assert L.splitkv_backward_kernel(4, 3, 128, 128, 1) < 0
+    assert k.splitkv_backward_kernel(32, 8, 128, 256, k.SPLITKV_BF16) == k.KERNEL_TC
+    assert k.splitkv_backward_kernel(32, 8, 64, 256, k.SPLITKV_BF16) == k.KERNEL_SIMT
+    assert k.splitkv_backward_kernel(4, 4, 128, 128, k.SPLITKV_F32) == k.KERNEL_SIMT
 
 
 def test_work_buffer_too_small_is_capacity_error(k):
