@@ -354,6 +354,8 @@ def run_backward(args, dctx, w, inp, run, out, lse, acc):
     K timed backward steps.  Algorithmic flops = 2.5 x forward (QK^T recompute, dP, dV, dQ, dK)."""
     import torch
 
+    from context_long_attention_lpt_gb300 import splitkv as K
+
     g = torch.Generator(device=out.device).manual_seed(0)
     dout = torch.randn(out.shape, generator=g, device=out.device, dtype=torch.float32).to(out.dtype)
     for _ in range(2):
