@@ -60,8 +60,12 @@ constexpr int kThreads = 384;
 // 2 x 128 x 216 + 128 x 72 = 64512 (per SM sub-partition 216 + 216 + 72 <= 512).
 constexpr int kRegsSoftmax = 216, kRegsOther = 72;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kSyncWarp = 10;
-// named barriers between the sync warp and the MMA warp (0 is __syncthreads)
-constexpr int kBarReadyA = 1, kBarReadyB = 2;
+// Named barriers (0 is __syncthreads).  The MMA warp syncs on each; the others
+// only arrive:  Q and K(0) ready (sync warp);  tile t of query tile A ready:
+// P_A(t) written (the four softmax warps of A) and V(t), K(t+1) landed (sync
+// warp);  P_B(t) written (the four softmax warps of B).
+constexpr int kBarPrologue = 1, kBarTileA = 2, kBarTileB = 3;
+constexpr int kBarPrologueThreads = 64, kBarTileAThreads = 192, kBarTileBThreads = 160;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
 constexpr uint32_t kTmemCols = 512;
@@ -81,10 +85,10 @@ struct Barriers {
   // MMA to read either, so one softmax thread of that tile arrives once it has
   // seen S(j) complete (MMAs complete in issue order).
   uint64_t kv_free[kStages];
-  uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
+  uint64_t s_full[2], o_done[2];  // per query tile
   uint64_t drain;
   uint32_t tmem_base;
-  uint32_t abort;  // set by the sync warp when a wait timed out
+  uint32_t abort;  // set by a warp whose wait timed out, before its last arrival
 };
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (2 + 2 * kStages) + sizeof(Barriers);
@@ -185,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(&bar->s_full[x], 1);
-      ptx::mbar_init(&bar->p_full[x], 4);
       ptx::mbar_init(&bar->o_done[x], 1);
     }
     ptx::mbar_init(&bar->drain, 1);
@@ -279,39 +282,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     const int nx = has_b ? 2 : 1;
-    auto handoff = [&](int id) { asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory"); };
-    auto take = [&](int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); };
     if (warp == kSyncWarp) {
       // ------------------------------------------------------------ sync warp
-      // Hands over, in order: Q and K(0) ready; then per tile t: V(t), K(t+1)
-      // and P_A(t) ready (barrier A), P_B(t) ready (barrier B).  Warp 9 takes
-      // each hand-off once, so this warp never runs a hand-off ahead: the next
-      // one needs a P that exists only after warp 9 used the previous one.
-      // On a timeout it flags the abort, hands off once more and stops.
+      // Arrives, in order: once Q and K(0) have landed; then per tile t once
+      // V(t) and K(t+1) have.  Before its tile-t arrival it also sees S_A(t)
+      // complete: S_A(t) is issued only after the MMA warp passed barrier A of
+      // tile t-1, so no arrival of this warp can count toward an earlier tile
+      // (the K/V ring alone would let it run a tile ahead).  On a timeout it
+      // flags the abort, arrives once more and stops.
       bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
       int32_t nv_cur = 0, nv_next = 0;
       bool has_cur = ok && next_tile(&nv_cur);
       if (has_cur) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
       if (!ok && lane == 0) bar->abort = 1;
       __syncwarp();
-      handoff(kBarReadyA);
+      ptx::bar_arrive(kBarPrologue, kBarPrologueThreads);
       int32_t t = 0;
       while (ok && has_cur) {
         const bool has_next = next_tile(&nv_next);
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[t % kStages], (t / kStages) & 1));
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[0], t & 1));
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[t % kStages], (t / kStages) & 1));
         if (ok && has_next)
           ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1));
-        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[0], t & 1));
         if (!ok && lane == 0) bar->abort = 1;
         __syncwarp();
-        handoff(kBarReadyA);
-        if (!ok) break;
-        if (nx == 2) {
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->p_full[1], t & 1));
-          if (!ok && lane == 0) bar->abort = 1;
-          __syncwarp();
-          handoff(kBarReadyB);
-        }
+        ptx::bar_arrive(kBarTileA, kBarTileAThreads);
         ++t;
         has_cur = has_next;
         nv_cur = nv_next;
@@ -319,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     } else {
     // ------------------------------------------------------------------ MMA
-    // Lane 0 issues every tcgen05.mma and commit; the warp takes the sync
-    // warp's hand-offs (a named barrier: far cheaper than an mbarrier wait,
-    // and the tensor pipe drains while the issuing thread waits).  Commits
-    // are kept to two a tile.
+    // Lane 0 issues every tcgen05.mma and commit; the warp learns that a tile is
+    // ready from a named barrier (far cheaper than an mbarrier wait, and the
+    // tensor pipe drains while the issuing thread waits).  Commits are kept
+    // to two a tile.
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
     // Descriptors of every operand tile, built once; an MMA only adds an offset.
@@ -344,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* abort_flag = &bar->abort;
     int32_t nv_cur = 0, nv_next = 0;
     bool has_cur = next_tile(&nv_cur);
-    take(kBarReadyA);  // Q, K(0)
+    ptx::bar_sync(kBarPrologue, kBarPrologueThreads);  // Q, K(0)
     bool ok = *abort_flag == 0;
     int32_t t = 0;
     if (ok && has_cur) {
@@ -357,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (has_cur && ok) {
       const bool has_next = next_tile(&nv_next);
       const int vs = t % kStages;
-      take(kBarReadyA);  // V(t), K(t+1), P_A(t)
+      ptx::bar_sync(kBarTileA, kBarTileAThreads);  // V(t), K(t+1), P_A(t)
       if (*abort_flag != 0) { ok = false; break; }
       uint8_t* vtile = sv + vs * kTileBytes;
       const int ksteps = (nv_cur + 15) >> 4;
@@ -375,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < nx; ++x) {
         // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
         if (x == 1) {
-          take(kBarReadyB);  // P_B(t)
+          ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t)
           if (*abort_flag != 0) { ok = false; break; }
         }
         tc::fence_after_sync();
@@ -440,7 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t pos0 = lo + off;
         const int32_t nvalid = min(kN, n - off);
         // waits and TMEM accesses stay warp-uniform (tcgen05.ld/st are warp-collective)
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1))) {
+          // the MMA warp may be waiting for this tile: flag the abort, arrive, stop
+          if (lane == 0) bar->abort = 1;
+          __syncwarp();
+          ptx::bar_arrive(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
+          ok = false;
+          break;
+        }
         if (release_kv && lane == 0) ptx::mbar_arrive(&bar->kv_free[t % kStages]);  // release t
         tc::fence_after_sync();
         uint32_t sr[4][32];
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_t overwrites P_{t-1}, which PV_{t-1} read: done, as it was issued
         // before S_t, which has completed.
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar->p_full[x]);
+        ptx::bar_arrive(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
       }
     }
     // epilogue: O / l and the log-sum-exp of this row; o_done_x is committed
