@@ -38,6 +38,7 @@ class SplitKVAttention:
         self.dcp_alpha, self.dcp_beta, self.dcp_gamma = float(dcp_alpha), float(dcp_beta), float(dcp_gamma)
         self.n_shards_used = self.n_shards
         self._tickets = None
+        self._grad_pools = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
         self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
@@ -121,13 +122,19 @@ class SplitKVAttention:
 
     def backward(self, q, k_pool, v_pool, block_table, scale, out, lse, dout, stream=None):
         """Gradients of the forward pass that produced (out, lse) for upstream gradient dout.
-        Returns (dq fp32 [total_q, Hq, d], dk_pool, dv_pool fp32 like the pools; zero where no key)."""
+        Returns (dq fp32 [total_q, Hq, d], dk_pool, dv_pool fp32 like the pools; zero where no key).
+        dk_pool / dv_pool are this object's buffers, rewritten by the next call: every key slot is
+        written by every call and the slots without a key stay zero, so they are cleared only when
+        the pool shape or the block table (storage or in-place version) changes."""
         dev = q.device
         delta = torch.empty((self.total_q, self.Hq), dtype=torch.float32, device=dev)
         _k.splitkv_bwd_delta(out, dout, delta, stream=stream)
         dq_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32, device=dev)
-        dk = torch.zeros(tuple(k_pool.shape), dtype=torch.float32, device=dev)
-        dv = torch.zeros(tuple(v_pool.shape), dtype=torch.float32, device=dev)
+        key = (tuple(k_pool.shape), dev, block_table.data_ptr(), block_table._version)
+        if self._grad_pools is None or self._grad_pools[0] != key:
+            self._grad_pools = (key, torch.zeros(tuple(k_pool.shape), dtype=torch.float32, device=dev),
+                                torch.zeros(tuple(v_pool.shape), dtype=torch.float32, device=dev))
+        dk, dv = self._grad_pools[1], self._grad_pools[2]
         _k.splitkv_attn_backward(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
                                  self.total_q, self.max_q_len, self.block_len, scale, self.causal, dout, lse,
                                  delta, dq_part, dk, dv, stream=stream)

@@ -52,11 +52,11 @@ def test_backward_is_deterministic_in_dk_dv_and_close_in_dq():
     w = SMALL["varlen_small"]
     inp, run, out, lse = run_cuda(w)
     dout = torch.ones_like(out)
-    a = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+    a = [x.clone() for x in run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)]
     b = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
     torch.cuda.synchronize()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])  # dK / dV: no atomics
-    assert (a[0] - b[0]).abs().max().item() < 1e-4  # dQ: fp32 atomics, order may differ
+    assert (a[0] - b[0]).abs().max().item() < 1e-4  # dQ: fp32 atomics on the CUDA-core path
 
 
 @pytest.mark.parametrize("name", ["shortq", "largest", "decode"])
