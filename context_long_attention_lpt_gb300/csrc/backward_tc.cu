@@ -392,19 +392,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ========================================================== dK / dV kernel
 
-constexpr int kKeySplit = 16;  // CTAs per (item, K/V head); each takes every 16th key tile
+constexpr int kKeySplit = 16;   // CTAs per (item, K/V head); each takes every 16th key tile
+constexpr int kRowsB = 64;      // query rows per tile here: two tiles' S^T / dP^T fit in TMEM
+constexpr int kQdStages = 4;    // Q / dO ring: the tile in the elementwise pass, the next one's
+                                // S^T / dP^T in the pipe, and two loading
+constexpr uint32_t kHalf64 = kRowsB * 128;         // 64 rows x 64 bf16 (one swizzled half)
+constexpr uint32_t kTile64 = 2 * kHalf64;          // 64 x 128 bf16
+// TMEM: S^T of row-tile parity b at 64 b, dP^T at 128 + 64 b; dV and dK as in the dQ kernel
+constexpr uint32_t kColST = 0, kColDPT = 128;
+
+__device__ __forceinline__ uint32_t kstep_off64(int kk) { return ((kk >> 2) * kHalf64 + (kk & 3) * 32) >> 4; }
 
 struct KvBarriers {
-  uint64_t kv_full;              // K and V of the current key tile
-  uint64_t qd_full[kStages];     // Q, dO (TMA) and L, D (producer lanes) of a row tile
-  uint64_t qd_free[kStages];     // the row tile's dV / dK MMAs have read Q and dO
-  uint64_t s_full, ds_full;      // S^T, dP^T in TMEM; P^T, dS^T written back
-  uint64_t o_done;               // the key tile's last dV / dK MMA completed
+  uint64_t kv_full;                 // K and V of the current key tile
+  uint64_t qd_full[kQdStages];      // Q, dO (TMA) and L, D (producer lanes) of a row tile
+  uint64_t qd_free[kQdStages];      // the row tile's dV / dK MMAs have read Q and dO
+  uint64_t s_full[2], ds_full[2];   // per row-tile parity: S^T, dP^T ready; P^T, dS^T written back
+  uint64_t o_done;                  // the key tile's last dV / dK MMA completed
   uint64_t drain;
   uint32_t tmem_base;
-  float ld[kStages][2][kRows];   // L and D of the row tile's rows
+  float ld[kQdStages][2][kRowsB];   // L and D of the row tile's rows
 };
-constexpr size_t kKvSmem = 1024 + kTileBytes * (2 + 2 * kStages) + sizeof(KvBarriers);
+constexpr size_t kKvSmem = 1024 + 2 * kTileBytes + 2 * kQdStages * kTile64 + sizeof(KvBarriers);
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -413,11 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sk = smem;                        // K tile
-  uint8_t* sv = smem + kTileBytes;           // V tile
-  uint8_t* sq = smem + 2 * kTileBytes;       // Q ring
-  uint8_t* sdo = sq + kStages * kTileBytes;  // dO ring
-  KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kStages * kTileBytes);
+  uint8_t* sk = smem;                          // K tile
+  uint8_t* sv = smem + kTileBytes;             // V tile
+  uint8_t* sq = smem + 2 * kTileBytes;         // Q ring
+  uint8_t* sdo = sq + kQdStages * kTile64;     // dO ring
+  KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kQdStages * kTile64);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t split = static_cast<int32_t>(blockIdx.x % kKeySplit);
@@ -431,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
-  const int32_t n_rt = (rows + kRows - 1) / kRows;  // row tiles of the sequence
+  const int32_t n_rt = (rows + kRowsB - 1) / kRowsB;  // row tiles of the sequence
   // every key below kv_len gets a gradient (zero if no row sees it)
   TileSeq tiles;
   tiles.ib = ItemBlocks{wv.blocks() + __ldg(it + kItBlockOff),
@@ -448,12 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar->kv_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kQdStages; ++s) {
       ptx::mbar_init(&bar->qd_full[s], 1);
       ptx::mbar_init(&bar->qd_free[s], 1);
     }
-    ptx::mbar_init(&bar->s_full, 1);
-    ptx::mbar_init(&bar->ds_full, 4);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&bar->s_full[b], 1);
+      ptx::mbar_init(&bar->ds_full[b], 4);
+    }
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
@@ -493,14 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_3d(sv + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->kv_full);
       }
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
-        const int s = rt % kStages;
-        if (rt >= kStages && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_free[s], ((rt - kStages) / kStages) & 1))) {
+        const int s = rt % kQdStages;
+        if (rt >= kQdStages &&
+            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_free[s], ((rt - kQdStages) / kQdStages) & 1))) {
           ok = false;
           break;
         }
-        // L and D of rows r*128 .. r*128+127 (rows past the sequence: L = -inf)
-        for (int i = lane; i < kRows; i += 32) {
-          const int32_t row = r * kRows + i;
+        // L and D of rows r*64 .. r*64+63 (rows past the sequence: L = -inf)
+        for (int i = lane; i < kRowsB; i += 32) {
+          const int32_t row = r * kRowsB + i;
           float L = -INFINITY, Dv = 0.f;
           if (row < rows) {
             const int64_t g = static_cast<int64_t>(cu_q + row / G) * a.Hq + kvh * G + row % G;
@@ -512,12 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          const int32_t tok0 = cu_q + (r * kRows) / G;
-          ptx::mbar_arrive_expect_tx(&bar->qd_full[s], 2 * kTileBytes);
-          ptx::tma_load_3d(sq + s * kTileBytes, &tmap_q, 0, kvh * G, tok0, &bar->qd_full[s]);
-          ptx::tma_load_3d(sq + s * kTileBytes + kHalfBytes, &tmap_q, 64, kvh * G, tok0, &bar->qd_full[s]);
-          ptx::tma_load_3d(sdo + s * kTileBytes, &tmap_do, 0, kvh * G, tok0, &bar->qd_full[s]);
-          ptx::tma_load_3d(sdo + s * kTileBytes + kHalfBytes, &tmap_do, 64, kvh * G, tok0, &bar->qd_full[s]);
+          const int32_t tok0 = cu_q + (r * kRowsB) / G;
+          ptx::mbar_arrive_expect_tx(&bar->qd_full[s], 2 * kTile64);
+          ptx::tma_load_3d(sq + s * kTile64, &tmap_q, 0, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sq + s * kTile64 + kHalf64, &tmap_q, 64, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sdo + s * kTile64, &tmap_do, 0, kvh * G, tok0, &bar->qd_full[s]);
+          ptx::tma_load_3d(sdo + s * kTile64 + kHalf64, &tmap_do, 64, kvh * G, tok0, &bar->qd_full[s]);
         }
       }
       ++kt;
@@ -527,62 +539,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every copy issued has landed before shared memory is released
     if (lane == 0) {
       if (kt > 0 && !ptx::mbar_wait(&bar->kv_full, (kt - 1) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
-      for (int32_t v = max(0, rt - kStages); v < rt; ++v)
-        if (!ptx::mbar_wait(&bar->qd_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, rt - kQdStages); v < rt; ++v)
+        if (!ptx::mbar_wait(&bar->qd_full[v % kQdStages], (v / kQdStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    // Per row tile: S^T = K Q^T, dP^T = V dO^T; once the key threads have put
-    // P^T and dS^T over them: dV += P^T dO, dK += dS^T Q.  The next row tile's
-    // S^T is issued after those, which read the same columns (MMAs run in order).
-    const uint32_t idesc_s = tc::idesc_bf16_f32(kN, kRows, false, false);
+    // Row tile r uses the TMEM pair of parity b = r & 1.  S^T(r+1), dP^T(r+1)
+    // are issued before waiting for the key threads' pass over tile r, so the
+    // pipe works while they run; then dV += P^T(r) dO(r), dK += dS^T(r) Q(r).
+    // S^T(r+2) reuses tile r's columns and is issued after those MMAs (in order).
+    const uint32_t idesc_s = tc::idesc_bf16_f32(kN, kRowsB, false, false);
     const uint32_t idesc_acc = tc::idesc_bf16_f32(kN, kD, false, true);
     const tc::Desc dk = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
     const tc::Desc dv = tc::split(tc::smem_desc(ptx::smem_addr(sv), 16, 1024, tc::kSwizzle128B));
     const tc::Desc dq = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
     const tc::Desc ddo = tc::split(tc::smem_desc(ptx::smem_addr(sdo), 16, 1024, tc::kSwizzle128B));
-    const tc::Desc dq_mn = tc::split(tc::smem_desc(ptx::smem_addr(sq), kHalfBytes, 1024, tc::kSwizzle128B));
-    const tc::Desc ddo_mn = tc::split(tc::smem_desc(ptx::smem_addr(sdo), kHalfBytes, 1024, tc::kSwizzle128B));
+    const tc::Desc dq_mn = tc::split(tc::smem_desc(ptx::smem_addr(sq), kHalf64, 1024, tc::kSwizzle128B));
+    const tc::Desc ddo_mn = tc::split(tc::smem_desc(ptx::smem_addr(sdo), kHalf64, 1024, tc::kSwizzle128B));
+    // S^T, dP^T of the row tile in ring slot s into the TMEM pair b
+    auto issue_s = [&](int s, int b) {
+      const uint32_t qoff = s * (kTile64 >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_ss_fast(tmem + kColST + 64 * b, dk, kstep_off(kk), dq, qoff + kstep_off64(kk), idesc_s, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_ss_fast(tmem + kColDPT + 64 * b, dv, kstep_off(kk), ddo, qoff + kstep_off64(kk), idesc_s, kk > 0);
+      tc::commit(&bar->s_full[b]);
+    };
     TileSeq walk = tiles;
     int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
     bool ok = true;
     while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full, kt & 1))) {
-        ok = false;
-        break;
-      }
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full, kt & 1)) &&
+           __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rt % kQdStages], (rt / kQdStages) & 1));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (lane == 0) issue_s(rt % kQdStages, rt & 1);
+      __syncwarp();
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
-        const int s = rt % kStages;
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kStages) & 1))) {
-          ok = false;
-          break;
+        const int s = rt % kQdStages, b = rt & 1;
+        if (r + 1 < n_rt) {
+          const int32_t rn = rt + 1;
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rn % kQdStages], (rn / kQdStages) & 1))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          if (lane == 0) issue_s(rn % kQdStages, rn & 1);
+          __syncwarp();
         }
-        tc::fence_after_sync();
-        const uint32_t qoff = s * kTile16;
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            tc::mma_ss_fast(tmem + kColS, dk, kstep_off(kk), dq, qoff + kstep_off(kk), idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            tc::mma_ss_fast(tmem + kColDP, dv, kstep_off(kk), ddo, qoff + kstep_off(kk), idesc_s, kk > 0);
-          tc::commit(&bar->s_full);
-        }
-        __syncwarp();
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full, rt & 1))) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full[b], (rt >> 1) & 1))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         if (lane == 0) {
+          const uint32_t qoff = s * (kTile64 >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColS + 8 * kk, ddo_mn, qoff + kk * (2048 >> 4), idesc_acc,
-                            (r > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kRowsB / 16; ++kk)
+            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColST + 64 * b + 8 * kk, ddo_mn, qoff + kk * (2048 >> 4),
+                            idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDP + 8 * kk, dq_mn, qoff + kk * (2048 >> 4), idesc_acc,
-                            (r > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kRowsB / 16; ++kk)
+            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDPT + 64 * b + 8 * kk, dq_mn, qoff + kk * (2048 >> 4),
+                            idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&bar->qd_free[s]);
           if (r == n_rt - 1) tc::commit(&bar->o_done);
         }
@@ -607,51 +628,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       // causal: the row (token t, head) sees this key iff t >= pos - (kv_len - q_len)
       const int32_t t_first = a.causal ? max(0, pos0 + k - (kv_len - q_len)) : 0;
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
-        const int s = rt % kStages;
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kStages) & 1)) ||
-            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full, rt & 1))) {
+        const int s = rt % kQdStages, b = rt & 1;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kQdStages) & 1)) ||
+            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[b], (rt >> 1) & 1))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         // rows j of the tile this key contributes to: [jmin, jmax)
-        const int32_t jmin = key_valid ? max(0, t_first * G - r * kRows) : kRows;
-        const int32_t jmax = min(kRows, rows - r * kRows);
+        const int32_t jmin = key_valid ? max(0, t_first * G - r * kRowsB) : kRowsB;
+        const int32_t jmax = min(kRowsB, rows - r * kRowsB);
         const float* Ls = bar->ld[s][0];
         const float* Ds = bar->ld[s][1];
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sr[2][32], dp[2][32], pk[32], dk2[32];
-          tc::tmem_ld32(lane_addr + kColS + 64 * hh, sr[0]);
-          tc::tmem_ld32(lane_addr + kColS + 64 * hh + 32, sr[1]);
-          tc::tmem_ld32(lane_addr + kColDP + 64 * hh, dp[0]);
-          tc::tmem_ld32(lane_addr + kColDP + 64 * hh + 32, dp[1]);
-          tc::tmem_ld_wait();
+        uint32_t sr[2][32], dp[2][32], pk[32], dk2[32];
+        tc::tmem_ld32(lane_addr + kColST + 64 * b, sr[0]);
+        tc::tmem_ld32(lane_addr + kColST + 64 * b + 32, sr[1]);
+        tc::tmem_ld32(lane_addr + kColDPT + 64 * b, dp[0]);
+        tc::tmem_ld32(lane_addr + kColDPT + 64 * b + 32, dp[1]);
+        tc::tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float p[2], ds[2];
+          for (int i = 0; i < 32; i += 2) {
+            float p[2], ds[2];
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int j = 64 * hh + 32 * q + i + e;
-                const float Lj = Ls[j];
-                const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
-                const float pj = fast_exp2(__uint_as_float(sr[q][i + e]) * c - Lj * kLog2e);
-                p[e] = on ? pj : 0.f;
-                ds[e] = on ? pj * (__uint_as_float(dp[q][i + e]) - Ds[j]) : 0.f;
-              }
-              pk[16 * q + i / 2] = pack_bf16(p[0], p[1]);
-              dk2[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+            for (int e = 0; e < 2; ++e) {
+              const int j = 32 * q + i + e;
+              const float Lj = Ls[j];
+              const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
+              const float pj = fast_exp2(__uint_as_float(sr[q][i + e]) * c - Lj * kLog2e);
+              p[e] = on ? pj : 0.f;
+              ds[e] = on ? pj * (__uint_as_float(dp[q][i + e]) - Ds[j]) : 0.f;
             }
-          // P^T over S^T columns, dS^T over dP^T columns [32 hh, 32 hh + 32): all already read
-          tc::tmem_st32(lane_addr + kColS + 32 * hh, pk);
-          tc::tmem_st32(lane_addr + kColDP + 32 * hh, dk2);
-        }
+            pk[16 * q + i / 2] = pack_bf16(p[0], p[1]);
+            dk2[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+          }
+        // P^T over the S^T columns, dS^T over the dP^T columns (first 32 of 64: all already read)
+        tc::tmem_st32(lane_addr + kColST + 64 * b, pk);
+        tc::tmem_st32(lane_addr + kColDPT + 64 * b, dk2);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar->ds_full);
+        if (lane == 0) ptx::mbar_arrive(&bar->ds_full[b]);
       }
       if (!ok) break;
       // epilogue: this key's dV and dK = scale * sum dS^T Q
@@ -689,12 +707,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int make_maps(const PartialArgs& a, const void* dout, CUtensorMap* tq, CUtensorMap* tdo, CUtensorMap* tk,
+// Maps over q / dout ([total_q, Hq, d]: boxes of `rows` query rows = rows / G
+// tokens x the G heads of a K/V head) and the K / V pools (128-key boxes).
+int make_maps(const PartialArgs& a, const void* dout, int rows, CUtensorMap* tq, CUtensorMap* tdo, CUtensorMap* tk,
               CUtensorMap* tv) {
   const int32_t G = a.Hq / a.Hkv;
   const uint64_t qdims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
   const uint64_t qstrides[2] = {kD * 2ull, static_cast<uint64_t>(a.Hq) * kD * 2ull};
-  const uint32_t qbox[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kRows / G)};
+  const uint32_t qbox[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(rows / G)};
   int st = encode_bf16_3d(tq, a.q, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == SPLITKV_OK) st = encode_bf16_3d(tdo, dout, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
   const uint64_t kdims[3] = {kD, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.n_pool_blocks) * a.block_len};
@@ -710,7 +730,7 @@ int make_maps(const PartialArgs& a, const void* dout, CUtensorMap* tq, CUtensorM
 bool bwd_tc_supports(const PartialArgs& a) {
   if (a.dtype != SPLITKV_BF16 || a.d != kD || a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
   const int32_t G = a.Hq / a.Hkv;
-  return G >= 1 && G <= kRows && kRows % G == 0 && a.block_len % kN == 0 &&
+  return G >= 1 && G <= kRowsB && kRowsB % G == 0 && a.block_len % kN == 0 &&
          static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
 }
 
@@ -721,8 +741,9 @@ int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, cons
   const int64_t grid = static_cast<int64_t>(units) * a.Hkv * a.n_items;
   if (grid == 0) return SPLITKV_OK;
   if (grid > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many backward units");
-  CUtensorMap tq, tdo, tk, tv;
-  int st = make_maps(a, dout, &tq, &tdo, &tk, &tv);
+  CUtensorMap tq, tdo, tk, tv, tq64, tdo64, tk2, tv2;
+  int st = make_maps(a, dout, kRows, &tq, &tdo, &tk, &tv);
+  if (st == SPLITKV_OK) st = make_maps(a, dout, kRowsB, &tq64, &tdo64, &tk2, &tv2);
   if (st != SPLITKV_OK) return st;
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDqSmem));
@@ -736,7 +757,7 @@ int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, cons
   e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKvSmem));
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward smem attribute: %s", cudaGetErrorString(e));
   bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kThreads, kKvSmem, stream>>>(a, lse, delta, dk_pool, dv_pool,
-                                                                                     tq, tdo, tk, tv);
+                                                                                     tq64, tdo64, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dK/dV launch: %s", cudaGetErrorString(e));
   return SPLITKV_OK;

@@ -242,7 +242,7 @@ int splitkv_bwd_delta(const void* o, const void* dout, int32_t total_q, int32_t 
                       int32_t dtype, float* delta, void* stream);
 
 /* Per-shard backward over the work items of splitkv_build_work.  Tensor cores
- * (tcgen05) for bf16, d = 128, block_len % 128 == 0 and Hq/Hkv dividing 128;
+ * (tcgen05) for bf16, d = 128, block_len % 128 == 0 and Hq/Hkv dividing 64;
  * CUDA cores otherwise.
  * In (device): q, k_pool, v_pool, block_table, work as for the forward; dout
  * [total_q, Hq, d] (dtype); lse fp32 [total_q, Hq] (splitkv_merge's lse_out);
