@@ -13,7 +13,8 @@
 // Two kernels:
 //  * bwd_dq_tc_kernel: one CTA per (work item, K/V head, 128 query rows).  It
 //    walks the item's key tiles like the forward: S = Q K^T and dP = dO V^T in
-//    TMEM, the row threads form dS (bf16) over S, then dQ += dS K.
+//    TMEM, the row threads form dS (bf16) over S, then dQ += dS K.  S is double
+//    buffered, so the next tile's S MMAs run during the row threads' pass.
 //  * bwd_dkdv_tc_kernel: one CTA per (work item, K/V head, a stride of the
 //    item's 128-key tiles).  Keys sit in the TMEM lanes: S^T = K Q^T and
 //    dP^T = V dO^T, the key threads form P^T and dS^T (bf16) in place, then
@@ -37,17 +38,15 @@ namespace {
 constexpr int kD = 128;
 constexpr int kRows = 128;  // query rows per tile
 constexpr int kN = 128;     // keys per tile
-constexpr int kStages = 2;
 constexpr uint32_t kHalfBytes = 128 * 64 * 2;    // 128 rows x 64 bf16: one swizzled half
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile
-constexpr uint32_t kTile16 = kTileBytes >> 4;    // in descriptor address units
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 192;  // warps 0-3: elementwise (one TMEM lane each); 4: TMA; 5: MMA
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 
-// TMEM columns (both kernels): scores, dP, then one or two fp32 accumulators.
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
+// TMEM columns of the dK/dV kernel's two fp32 accumulators.
+constexpr uint32_t kColAcc0 = 256, kColAcc1 = 384;
 
 // Byte offset (>> 4) of 16-wide K step kk inside a K-major SW128 tile made of two
 // 64-column halves: steps 0-3 in the first half, 4-7 in the second.
@@ -122,14 +121,21 @@ struct TileSeq {
 
 // ============================================================== dQ kernel
 
+constexpr int kKStages = 3;  // K(t) is read by S(t) and, after the row threads' pass, by dQ(t)
+constexpr int kVStages = 2;  // V(t) only by dP(t)
+// TMEM: S of tile parity b at 128 b (dS is written over it), dP, then dQ
+constexpr uint32_t kColS0 = 0, kColDPq = 256, kColDQ = 384;
+
 struct DqBarriers {
-  uint64_t qd_full;                  // Q and dO tiles of the unit
-  uint64_t kv_full[kStages];         // K(t) and V(t)
-  uint64_t kv_free[kStages];         // the slot's dQ MMA has read K(t)
-  uint64_t s_full, ds_full, o_done, drain;
+  uint64_t qd_full;                               // Q and dO tiles of the unit
+  uint64_t k_full[kKStages], k_free[kKStages];    // K(t); its dQ MMA has read it
+  uint64_t v_full[kVStages], v_free[kVStages];    // V(t); its dP MMA has read it
+  uint64_t s_full[2];                             // S of tile parity b ready
+  uint64_t dp_full, dp_free, ds_full;             // dP(t) ready; dP(t) read; dS(t) written
+  uint64_t o_done, drain;
   uint32_t tmem_base;
 };
-constexpr size_t kDqSmem = 1024 + kTileBytes * (2 + 2 * kStages) + sizeof(DqBarriers);
+constexpr size_t kDqSmem = 1024 + kTileBytes * (2 + kKStages + kVStages) + sizeof(DqBarriers);
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -138,11 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmap_v) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem;                       // Q tile
-  uint8_t* sdo = smem + kTileBytes;         // dO tile
-  uint8_t* sk = smem + 2 * kTileBytes;      // K ring
-  uint8_t* sv = sk + kStages * kTileBytes;  // V ring
-  DqBarriers* bar = reinterpret_cast<DqBarriers*>(sv + kStages * kTileBytes);
+  uint8_t* sq = smem;                        // Q tile
+  uint8_t* sdo = smem + kTileBytes;          // dO tile
+  uint8_t* sk = smem + 2 * kTileBytes;       // K ring
+  uint8_t* sv = sk + kKStages * kTileBytes;  // V ring
+  DqBarriers* bar = reinterpret_cast<DqBarriers*>(sv + kVStages * kTileBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u = blockIdx.x;
@@ -173,11 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar->qd_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&bar->kv_full[s], 1);
-      ptx::mbar_init(&bar->kv_free[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      ptx::mbar_init(&bar->k_full[s], 1);
+      ptx::mbar_init(&bar->k_free[s], 1);
     }
-    ptx::mbar_init(&bar->s_full, 1);
+    for (int s = 0; s < kVStages; ++s) {
+      ptx::mbar_init(&bar->v_full[s], 1);
+      ptx::mbar_init(&bar->v_free[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->s_full[b], 1);
+    ptx::mbar_init(&bar->dp_full, 1);
+    ptx::mbar_init(&bar->dp_free, 4);
     ptx::mbar_init(&bar->ds_full, 4);
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
@@ -208,29 +220,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t t = 0, pos0, nv, tok;
       bool ok = true;
       while (ok && tiles.next(&pos0, &nv, &tok)) {
-        const int s = t % kStages;
-        if (t >= kStages && !ptx::mbar_wait(&bar->kv_free[s], ((t - kStages) / kStages) & 1)) {
+        const int ks = t % kKStages, vs = t % kVStages;
+        if (t >= kKStages && !ptx::mbar_wait(&bar->k_free[ks], ((t - kKStages) / kKStages) & 1)) {
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
-        ptx::tma_load_3d(sk + s * kTileBytes, &tmap_k, 0, kvh, tok, &bar->kv_full[s]);
-        ptx::tma_load_3d(sk + s * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->kv_full[s]);
-        ptx::tma_load_3d(sv + s * kTileBytes, &tmap_v, 0, kvh, tok, &bar->kv_full[s]);
-        ptx::tma_load_3d(sv + s * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->kv_full[s]);
+        ptx::mbar_arrive_expect_tx(&bar->k_full[ks], kTileBytes);
+        ptx::tma_load_3d(sk + ks * kTileBytes, &tmap_k, 0, kvh, tok, &bar->k_full[ks]);
+        ptx::tma_load_3d(sk + ks * kTileBytes + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->k_full[ks]);
+        if (t >= kVStages && !ptx::mbar_wait(&bar->v_free[vs], ((t - kVStages) / kVStages) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&bar->v_full[vs], kTileBytes);
+        ptx::tma_load_3d(sv + vs * kTileBytes, &tmap_v, 0, kvh, tok, &bar->v_full[vs]);
+        ptx::tma_load_3d(sv + vs * kTileBytes + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->v_full[vs]);
         ++t;
       }
       if (!ok) atomicOr(a.status, ptx::kStatusTimeout);
       // every copy issued has landed before shared memory is released
       if (!ptx::mbar_wait(&bar->qd_full, 0)) atomicOr(a.status, ptx::kStatusTimeout);
-      for (int32_t v = max(0, t - kStages); v < t; ++v)
-        if (!ptx::mbar_wait(&bar->kv_full[v % kStages], (v / kStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, t - kKStages); v < t; ++v)
+        if (!ptx::mbar_wait(&bar->k_full[v % kKStages], (v / kKStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      for (int32_t v = max(0, t - kVStages); v < t; ++v)
+        if (!ptx::mbar_wait(&bar->v_full[v % kVStages], (v / kVStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    // Per tile t: S(t) = Q K(t)^T and dP(t) = dO V(t)^T; once the row threads
-    // have put dS(t) over S(t): dQ += dS(t) K(t).  S(t+1) is issued after
-    // dQ(t), which read dS(t) from the same columns (MMAs run in order).
+    // Tile t: S(t) = Q K(t)^T into the S buffer of parity t & 1, dP(t) = dO V(t)^T,
+    // and, once the row threads have put dS(t) over S(t), dQ += dS(t) K(t).
+    // dP(t+1) goes in as soon as the row threads have read dP(t) (halfway through
+    // their pass), ahead of dQ(t); S(t+2) follows dQ(t) into tile t's buffer
+    // (MMAs run in order, so dQ(t) has read dS(t) first).  The next tile's S and
+    // dP are thus done or in the pipe when the row threads finish a tile.
     const uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kN, false, false);
     const uint32_t idesc_dq = tc::idesc_bf16_f32(kRows, kD, false, true);
     const tc::Desc dq0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
@@ -238,40 +260,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const tc::Desc dk = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
     const tc::Desc dv = tc::split(tc::smem_desc(ptx::smem_addr(sv), 16, 1024, tc::kSwizzle128B));
     const tc::Desc dk_mn = tc::split(tc::smem_desc(ptx::smem_addr(sk), kHalfBytes, 1024, tc::kSwizzle128B));
-    auto issue_s_dp = [&](int32_t t) {
-      const uint32_t soff = (t % kStages) * kTile16;
+    constexpr uint32_t kTile16 = kTileBytes >> 4;
+    auto issue_s = [&](int32_t t) {
+      const uint32_t koff = (t % kKStages) * kTile16;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_ss_fast(tmem + kColS, dq0, kstep_off(kk), dk, soff + kstep_off(kk), idesc_s, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_ss_fast(tmem + kColDP, ddo, kstep_off(kk), dv, soff + kstep_off(kk), idesc_s, kk > 0);
-      tc::commit(&bar->s_full);
+        tc::mma_ss_fast(tmem + kColS0 + 128 * (t & 1), dq0, kstep_off(kk), dk, koff + kstep_off(kk), idesc_s, kk > 0);
+      tc::commit(&bar->s_full[t & 1]);
     };
+    auto issue_dp = [&](int32_t t) {
+      const int vs = t % kVStages;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_ss_fast(tmem + kColDPq, ddo, kstep_off(kk), dv, vs * kTile16 + kstep_off(kk), idesc_s, kk > 0);
+      tc::commit(&bar->dp_full);
+      tc::commit(&bar->v_free[vs]);
+    };
+    auto wait_all = [&](uint64_t* b, uint32_t parity) { return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity)); };
     TileSeq walk = tiles;
-    int32_t pos0, nv_cur = 0, nv_next = 0, tok;
-    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full, 0));
+    int32_t pos0, tok, nv_cur = 0, nv_next = 0, nv_next2 = 0;
+    bool ok = wait_all(&bar->qd_full, 0);
     bool has_cur = ok && walk.next(&pos0, &nv_cur, &tok);
-    int32_t t = 0;
+    bool has_next = has_cur && walk.next(&pos0, &nv_next, &tok);
     if (has_cur) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full[0], 0));
+      ok = wait_all(&bar->k_full[0], 0) && wait_all(&bar->v_full[0], 0);
       tc::fence_after_sync();
-      if (ok && lane == 0) issue_s_dp(0);
+      if (ok && lane == 0) {
+        issue_s(0);
+        issue_dp(0);
+      }
       __syncwarp();
+      if (ok && has_next) {
+        ok = wait_all(&bar->k_full[1 % kKStages], 0);
+        tc::fence_after_sync();
+        if (ok && lane == 0) issue_s(1);
+        __syncwarp();
+      }
     }
+    int32_t t = 0;
     while (has_cur && ok) {
-      const bool has_next = walk.next(&pos0, &nv_next, &tok);
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full, t & 1))) {
+      const bool has_next2 = has_next && walk.next(&pos0, &nv_next2, &tok);
+      if (has_next) {
+        if (!wait_all(&bar->dp_free, t & 1) || !wait_all(&bar->v_full[(t + 1) % kVStages], ((t + 1) / kVStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) issue_dp(t + 1);
+        __syncwarp();
+      }
+      if (!wait_all(&bar->ds_full, t & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const int s = t % kStages;
+      const int ks = t % kKStages;
       const int ksteps = (nv_cur + 15) >> 4;
       if (nv_cur < ksteps * 16) {
         // K rows of keys past the end inside the last 16-key step: zero (their dS
         // is 0, but the pool slot may hold anything); S(t) has read them already
-        uint8_t* ktile = sk + s * kTileBytes;
+        uint8_t* ktile = sk + ks * kTileBytes;
         for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
           const int cc = lane & 15;
           reinterpret_cast<uint4*>(ktile + (cc < 8 ? 0 : kHalfBytes) + r * 128)[cc & 7] = make_uint4(0, 0, 0, 0);
@@ -281,24 +329,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         for (int kk = 0; kk < ksteps; ++kk)
-          tc::mma_ts_fast(tmem + kColAcc0, tmem + kColS + 8 * kk, dk_mn, s * kTile16 + kk * (2048 >> 4), idesc_dq,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bar->kv_free[s]);
+          tc::mma_ts_fast(tmem + kColDQ, tmem + kColS0 + 128 * (t & 1) + 8 * kk, dk_mn,
+                          ks * kTile16 + kk * (2048 >> 4), idesc_dq, (t > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bar->k_free[ks]);
         if (!has_next) tc::commit(&bar->o_done);
       }
       __syncwarp();
-      if (has_next) {
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1))) {
+      if (has_next2) {
+        if (!wait_all(&bar->k_full[(t + 2) % kKStages], ((t + 2) / kKStages) & 1)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (lane == 0) issue_s_dp(t + 1);
+        if (lane == 0) issue_s(t + 2);
         __syncwarp();
       }
       ++t;
       has_cur = has_next;
+      has_next = has_next2;
       nv_cur = nv_next;
+      nv_next = nv_next2;
     }
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     if (lane == 0) tc::commit(&bar->drain);
@@ -320,20 +370,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t pos0, nvalid, tok, t = 0;
     bool ok = true;
     while (ok && walk.next(&pos0, &nvalid, &tok)) {
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full, t & 1))) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1)) ||
+          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->dp_full, t & 1))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
       const int32_t lim = live ? min(nvalid, my_vis - pos0) : 0;  // keys [0, lim) of the tile are seen
+      const uint32_t s_col = kColS0 + 128 * (t & 1);
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t sr[2][32], dp[2][32], pk[32];
-        tc::tmem_ld32(lane_addr + kColS + 64 * hh, sr[0]);
-        tc::tmem_ld32(lane_addr + kColS + 64 * hh + 32, sr[1]);
-        tc::tmem_ld32(lane_addr + kColDP + 64 * hh, dp[0]);
-        tc::tmem_ld32(lane_addr + kColDP + 64 * hh + 32, dp[1]);
+        tc::tmem_ld32(lane_addr + s_col + 64 * hh, sr[0]);
+        tc::tmem_ld32(lane_addr + s_col + 64 * hh + 32, sr[1]);
+        tc::tmem_ld32(lane_addr + kColDPq + 64 * hh, dp[0]);
+        tc::tmem_ld32(lane_addr + kColDPq + 64 * hh + 32, dp[1]);
         tc::tmem_ld_wait();
+        if (hh == 1) {  // all of dP(t) is in registers: the next dP may be issued
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bar->dp_free);
+        }
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -347,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
           }
-        // dS as bf16 over S columns [32 hh, 32 hh + 32): all already read
-        tc::tmem_st32(lane_addr + kColS + 32 * hh, pk);
+        // dS as bf16 over S columns [32 hh, 32 hh + 32) of this tile's buffer: all already read
+        tc::tmem_st32(lane_addr + s_col + 32 * hh, pk);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -365,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t acc[32];
       if (t > 0) {
-        tc::tmem_ld32(lane_addr + kColAcc0 + 32 * q4, acc);
+        tc::tmem_ld32(lane_addr + kColDQ + 32 * q4, acc);
         tc::tmem_ld_wait();
       }
       if (row_valid) {
