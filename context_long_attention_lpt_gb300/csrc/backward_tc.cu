@@ -134,6 +134,9 @@ struct DqBarriers {
   uint64_t dp_full, dp_free, ds_full;             // dP(t) ready; dP(t) read; dS(t) written
   uint64_t o_done, drain;
   uint32_t tmem_base;
+  // Tile t's key count | (tile t+1 exists) << 16 | (tile t+2 exists) << 17, at [t & 1]:
+  // written by row warp 0 before its dP(t)-read arrival, read by the MMA warp after it
+  uint32_t tinfo[2];
 };
 constexpr size_t kDqSmem = 1024 + kTileBytes * (2 + kKStages + kVStages) + sizeof(DqBarriers);
 
@@ -253,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // their pass), ahead of dQ(t); S(t+2) follows dQ(t) into tile t's buffer
     // (MMAs run in order, so dQ(t) has read dS(t) first).  The next tile's S and
     // dP are thus done or in the pipe when the row threads finish a tile.
+    // This lane's issue waits for the pipe, so every other wait here leaves the
+    // pipe idle: past the first two tiles the row threads, which have time to
+    // spare, wait for the V and K copies (V(t+1) before their dP(t)-read arrival,
+    // K(t+2) before their dS(t) arrival) and pass each tile's key count along.
     const uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kN, false, false);
     const uint32_t idesc_dq = tc::idesc_bf16_f32(kRows, kD, false, true);
     const tc::Desc dq0 = tc::split(tc::smem_desc(ptx::smem_addr(sq), 16, 1024, tc::kSwizzle128B));
@@ -277,11 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::commit(&bar->v_free[vs]);
     };
     auto wait_all = [&](uint64_t* b, uint32_t parity) { return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity)); };
+    int32_t pos0, tok, nv0 = 0, nv1 = 0;
     TileSeq walk = tiles;
-    int32_t pos0, tok, nv_cur = 0, nv_next = 0, nv_next2 = 0;
     bool ok = wait_all(&bar->qd_full, 0);
-    bool has_cur = ok && walk.next(&pos0, &nv_cur, &tok);
-    bool has_next = has_cur && walk.next(&pos0, &nv_next, &tok);
+    bool has_cur = ok && walk.next(&pos0, &nv0, &tok);
+    const bool has_one = has_cur && walk.next(&pos0, &nv1, &tok);
     if (has_cur) {
       ok = wait_all(&bar->k_full[0], 0) && wait_all(&bar->v_full[0], 0);
       tc::fence_after_sync();
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_dp(0);
       }
       __syncwarp();
-      if (ok && has_next) {
+      if (ok && has_one) {
         ok = wait_all(&bar->k_full[1 % kKStages], 0);
         tc::fence_after_sync();
         if (ok && lane == 0) issue_s(1);
@@ -299,16 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int32_t t = 0;
     while (has_cur && ok) {
-      const bool has_next2 = has_next && walk.next(&pos0, &nv_next2, &tok);
-      if (has_next) {
-        if (!wait_all(&bar->dp_free, t & 1) || !wait_all(&bar->v_full[(t + 1) % kVStages], ((t + 1) / kVStages) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (lane == 0) issue_dp(t + 1);
-        __syncwarp();
+      if (!wait_all(&bar->dp_free, t & 1)) {
+        ok = false;
+        break;
       }
+      tc::fence_after_sync();
+      const uint32_t info = bar->tinfo[t & 1];
+      const int32_t nv_cur = static_cast<int32_t>(info & 0xffffu);
+      const bool has_next = (info >> 16) & 1u, has_next2 = (info >> 17) & 1u;
+      if (has_next && lane == 0) issue_dp(t + 1);
+      __syncwarp();
       if (!wait_all(&bar->ds_full, t & 1)) {
         ok = false;
         break;
@@ -333,22 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ks * kTile16 + kk * (2048 >> 4), idesc_dq, (t > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar->k_free[ks]);
         if (!has_next) tc::commit(&bar->o_done);
+        if (has_next2) issue_s(t + 2);
       }
       __syncwarp();
-      if (has_next2) {
-        if (!wait_all(&bar->k_full[(t + 2) % kKStages], ((t + 2) / kKStages) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (lane == 0) issue_s(t + 2);
-        __syncwarp();
-      }
       ++t;
       has_cur = has_next;
-      has_next = has_next2;
-      nv_cur = nv_next;
-      nv_next = nv_next2;
     }
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     if (lane == 0) tc::commit(&bar->drain);
@@ -366,10 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = L != -INFINITY;  // a row with no visible key has no gradient
     const float c = a.scale * kLog2e, lc = live ? L * kLog2e : 0.f;
     const int32_t my_vis = row_valid ? visible_keys(q_len, kv_len, token, a.causal) : 0;
-    TileSeq walk = tiles;
-    int32_t pos0, nvalid, tok, t = 0;
+    TileSeq walk = tiles, ahead = tiles;  // ahead runs two tiles in front
+    int32_t pos0, nvalid, tok, apos, anv, atok, t = 0;
+    bool has1 = ahead.next(&apos, &anv, &atok);
+    bool has2 = has1 && ahead.next(&apos, &anv, &atok);  // tile 1 exists
+    bool has3 = has2 && ahead.next(&apos, &anv, &atok);  // tile 2 exists
     bool ok = true;
     while (ok && walk.next(&pos0, &nvalid, &tok)) {
+      const bool has_next = has2, has_next2 = has3;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1)) ||
           !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->dp_full, t & 1))) {
         ok = false;
@@ -387,6 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld32(lane_addr + kColDPq + 64 * hh + 32, dp[1]);
         tc::tmem_ld_wait();
         if (hh == 1) {  // all of dP(t) is in registers: the next dP may be issued
+          if (warp == 0) {
+            if (lane == 0)
+              bar->tinfo[t & 1] = static_cast<uint32_t>(nvalid) | (has_next ? 1u << 16 : 0u) |
+                                  (has_next2 ? 1u << 17 : 0u);
+            if (has_next && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[(t + 1) % kVStages],
+                                                                    ((t + 1) / kVStages) & 1)))
+              ok = false;
+          }
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&bar->dp_free);
@@ -407,10 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS as bf16 over S columns [32 hh, 32 hh + 32) of this tile's buffer: all already read
         tc::tmem_st32(lane_addr + s_col + 32 * hh, pk);
       }
+      if (warp == 1 && has_next2 &&
+          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 2) % kKStages], ((t + 2) / kKStages) & 1)))
+        ok = false;
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bar->ds_full);
+      has2 = has3;
+      has3 = has3 && ahead.next(&apos, &anv, &atok);
       ++t;
     }
     // epilogue: dQ = scale * sum dS K
