@@ -483,7 +483,10 @@ struct KvBarriers {
   uint32_t tmem_base;
   float ld[kQdStages][2][kRowsB];   // L and D of the row tile's rows
 };
-constexpr size_t kKvSmem = 1024 + 2 * kTileBytes + 2 * kQdStages * kTile64 + sizeof(KvBarriers);
+// Epilogue staging: each key warp passes 32 keys x 32 columns of dV or dK through
+// shared memory so that global stores go out as whole rows
+constexpr uint32_t kStageBytes = 4 * 32 * 32 * 4;
+constexpr size_t kKvSmem = 1024 + 2 * kTileBytes + 2 * kQdStages * kTile64 + kStageBytes + sizeof(KvBarriers);
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -496,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sv = smem + kTileBytes;             // V tile
   uint8_t* sq = smem + 2 * kTileBytes;         // Q ring
   uint8_t* sdo = sq + kQdStages * kTile64;     // dO ring
-  KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kQdStages * kTile64);
+  float* stage = reinterpret_cast<float*>(sdo + kQdStages * kTile64);  // epilogue staging
+  KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kQdStages * kTile64 + kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t split = static_cast<int32_t>(blockIdx.x % kKeySplit);
@@ -748,21 +752,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const int64_t krow = (static_cast<int64_t>(tok) + k) * a.Hkv + kvh;  // pool token tok + k
+      // Each chunk of 32 columns goes through this warp's 32 x 32 staging block
+      // (16-byte slot x of row k at x ^ (k & 7): no bank conflicts either way), then
+      // out as whole 128-byte row pieces, four keys per store instruction.
+      float4* wst = reinterpret_cast<float4*>(stage + warp * 32 * 32);
 #pragma unroll 1
       for (int q4 = 0; q4 < 8; ++q4) {
         const bool is_k = q4 >= 4;
         uint32_t acc[32];
         tc::tmem_ld32(lane_addr + (is_k ? kColAcc1 : kColAcc0) + 32 * (q4 & 3), acc);
         tc::tmem_ld_wait();
-        if (key_valid) {
-          const float f = is_k ? a.scale : 1.f;
-          float4* dst = reinterpret_cast<float4*>((is_k ? dk_pool : dv_pool) + krow * kD + 32 * (q4 & 3));
+        const float f = is_k ? a.scale : 1.f;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(acc[4 * i]) * f, __uint_as_float(acc[4 * i + 1]) * f,
-                                 __uint_as_float(acc[4 * i + 2]) * f, __uint_as_float(acc[4 * i + 3]) * f);
+        for (int i = 0; i < 8; ++i)
+          wst[lane * 8 + (i ^ (lane & 7))] =
+              make_float4(__uint_as_float(acc[4 * i]) * f, __uint_as_float(acc[4 * i + 1]) * f,
+                          __uint_as_float(acc[4 * i + 2]) * f, __uint_as_float(acc[4 * i + 3]) * f);
+        __syncwarp();
+        float* pool = is_k ? dk_pool : dv_pool;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int kr = 4 * i + (lane >> 3), x = lane & 7;  // key of the warp, 16-byte slot
+          const int key = warp * 32 + kr;
+          if (key < nv) {
+            const int64_t krow = (static_cast<int64_t>(tok) + key) * a.Hkv + kvh;  // pool token tok + key
+            reinterpret_cast<float4*>(pool + krow * kD + 32 * (q4 & 3))[x] = wst[kr * 8 + (x ^ (kr & 7))];
+          }
         }
+        __syncwarp();
       }
       ++kt;
     }
