@@ -431,22 +431,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     tc::fence_after_sync();
     const int64_t orow = static_cast<int64_t>(part_row + token) * a.Hq + h;
+    if (ok && t > 0) {
+      // The Q tile is free once o_done is seen (every S MMA has completed): each
+      // warp passes 32 rows x 32 columns at a time through its 4 KB of it (16-byte
+      // slot y of row k at y ^ (k & 7)) and stores whole 128-byte row pieces.
+      float4* wst = reinterpret_cast<float4*>(sq + warp * 4096);
+      int64_t orow_k[8];
+      bool valid_k[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int32_t rk = warp * 32 + 4 * i + (lane >> 3);
+        valid_k[i] = rk < n_rows;
+        orow_k[i] = static_cast<int64_t>(part_row + (r0 + rk) / G) * a.Hq + kvh * G + (r0 + rk) % G;
+      }
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t acc[32];
-      if (t > 0) {
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t acc[32];
         tc::tmem_ld32(lane_addr + kColDQ + 32 * q4, acc);
         tc::tmem_ld_wait();
-      }
-      if (row_valid) {
-        float4* dst = reinterpret_cast<float4*>(dq_part + orow * kD + 32 * q4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          wst[lane * 8 + (i ^ (lane & 7))] =
+              make_float4(__uint_as_float(acc[4 * i]) * a.scale, __uint_as_float(acc[4 * i + 1]) * a.scale,
+                          __uint_as_float(acc[4 * i + 2]) * a.scale, __uint_as_float(acc[4 * i + 3]) * a.scale);
+        __syncwarp();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (t > 0)
-            v = make_float4(__uint_as_float(acc[4 * i]) * a.scale, __uint_as_float(acc[4 * i + 1]) * a.scale,
-                            __uint_as_float(acc[4 * i + 2]) * a.scale, __uint_as_float(acc[4 * i + 3]) * a.scale);
-          dst[i] = v;
+          const int kr = 4 * i + (lane >> 3), y = lane & 7;
+          if (valid_k[i])
+            reinterpret_cast<float4*>(dq_part + orow_k[i] * kD + 32 * q4)[y] = wst[kr * 8 + (y ^ (kr & 7))];
+        }
+        __syncwarp();
+      }
+    } else {  // no key tile (the Q copy was never waited for) or the waits ran out: direct stores
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t acc[32];
+        if (t > 0) {
+          tc::tmem_ld32(lane_addr + kColDQ + 32 * q4, acc);
+          tc::tmem_ld_wait();
+        }
+        if (row_valid) {
+          float4* dst = reinterpret_cast<float4*>(dq_part + orow * kD + 32 * q4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t > 0)
+              v = make_float4(__uint_as_float(acc[4 * i]) * a.scale, __uint_as_float(acc[4 * i + 1]) * a.scale,
+                              __uint_as_float(acc[4 * i + 2]) * a.scale, __uint_as_float(acc[4 * i + 3]) * a.scale);
+            dst[i] = v;
+          }
         }
       }
     }

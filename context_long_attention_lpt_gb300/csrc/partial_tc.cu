@@ -536,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q_x's tile is free once o_done_x is seen (every MMA that reads it has
     // completed): each warp passes 32 rows x 32 columns at a time through its 4 KB
     // of it (16-byte slot y of row k at y ^ (k & 7): no bank conflicts either way)
-    // and stores whole 128-byte row pieces, four rows per instruction.
-    if (ok) {
+    // and stores whole 128-byte row pieces, four rows per instruction.  A unit with
+    // no key tile (t == 0) never waits for its Q copy, so it writes its zero rows
+    // directly, as does a unit whose waits ran out.
+    if (ok && t > 0) {
       float4* wst = reinterpret_cast<float4*>(sq + x * kTileBytes + wq * 4096);
       int64_t orow_k[8];
       bool valid_k[8];
@@ -570,6 +572,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<float4*>(a.o_part + orow_k[i] * kD + 32 * q4)[y] = wst[kr * 8 + (y ^ (kr & 7))];
         }
         __syncwarp();
+      }
+    } else {
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t orr[32];
+        if (t > 0) {
+          tc::tmem_ld32(o_addr + 32 * q4, orr);
+          tc::tmem_ld_wait();
+        }
+        if (row_valid) {
+          float4* dst = reinterpret_cast<float4*>(a.o_part + orow * kD + 32 * q4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t > 0 && l > 0.f)
+              v = make_float4(__uint_as_float(orr[4 * i]) * inv, __uint_as_float(orr[4 * i + 1]) * inv,
+                              __uint_as_float(orr[4 * i + 2]) * inv, __uint_as_float(orr[4 * i + 3]) * inv);
+            dst[i] = v;
+          }
+        }
       }
     }
     if (row_valid) a.lse_part[orow] = l > 0.f ? (m_used * c + __log2f(l)) * kLn2 : -INFINITY;
