@@ -19,7 +19,8 @@
 //    item's 128-key tiles).  Keys sit in the TMEM lanes: S^T = K Q^T and
 //    dP^T = V dO^T, the key threads form P^T and dS^T (bf16) in place, then
 //    dV += P^T dO and dK += dS^T Q accumulate over all query rows of the
-//    sequence, 128 at a time.
+//    sequence, 64 at a time (two row tiles' S^T | dP^T pairs fit in TMEM, so
+//    the next tile's MMAs run during the key threads' pass).
 // Every wait has a time limit; on expiry the status word gets bit 2 and the
 // CTA unwinds (all MMAs drained, TMEM freed).
 
