@@ -21,7 +21,7 @@ TOL = {"f32": 2e-4, "bf16": 2e-2}
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_small", "shortq_small", "varlen_small", "noncausal_multi_q",
-                                  "bf16_d64", "largest_small"])
+                                  "bf16_d64", "largest_small", "causal_empty_units"])
 def test_backward_matches_oracle(name):
     w = SMALL[name]
     inp, run, out, lse = run_cuda(w)

@@ -29,6 +29,9 @@ SMALL = {
     "noncausal_multi_q": wl.custom("shortq", causal=False, q_len=9, context=1000, block_len=128,
                                    n_shards=4),
     "bf16_d64": wl.custom("shortq", d=64, q_len=20, context=900, block_len=128, n_shards=3),
+    # causal queries longer than the context, one block per shard: the first query rows see
+    # none of the last blocks, so many (item, head, row tile) units have no key tile at all
+    "causal_empty_units": wl.custom("shortq", q_len=600, context=100, block_len=128, n_shards=6),
 }
 
 
@@ -64,7 +67,7 @@ def test_tensor_core_few_tile_items(seed):
 
 
 @pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
-@pytest.mark.parametrize("name", ["decode_small", "shortq_small", "varlen_small", "tiny"])
+@pytest.mark.parametrize("name", ["decode_small", "shortq_small", "varlen_small", "tiny", "causal_empty_units"])
 def test_partials_match_oracle_partials(name, kernel):
     """Each work item's (O_i, L_i) equals the oracle's partial over the oracle's own shard."""
     w = SMALL[name]
