@@ -9,6 +9,13 @@
 It owns the device buffers the calls need (work descriptor, partials, outputs),
 allocated with torch and reused across calls of the same shape.  It computes
 nothing itself.
+
+Streams: ``plan(stream=s)`` uploads the work descriptor on ``s`` (default: the
+current stream).  A device call on another stream first waits for that upload,
+and the next upload waits for the last device call that read the descriptor,
+so plans and calls may use different streams.  The partial buffers are shared
+by ``partial`` and ``merge``: calls of one batch on different streams are
+ordered by the caller, as with any stream API.
 """
 
 import numpy as np
@@ -50,11 +57,14 @@ class SplitKVAttention:
         self._work_dev = None
         self._o_part = None
         self._lse_part = None
+        self._upload = None    # (event, stream) of the last work upload
+        self._last_use = None  # event after the last device call that read the work buffer
         self.plan()
 
     # host steps -------------------------------------------------------------
-    def plan(self):
-        """Block costs, LPT plan and work lists on the host; copy the work to the device."""
+    def plan(self, stream=None):
+        """Block costs, LPT plan and work lists on the host; copy the work to the device on
+        ``stream`` (default: the current stream)."""
         self.block_cost = _k.splitkv_block_costs(self._q_len_np, self._kv_len_np, self.block_len,
                                                  self.causal)
         if self.planner == "lpt":
@@ -72,12 +82,19 @@ class SplitKVAttention:
             slot[1].synchronize()  # this buffer's last upload has left it
         if slot[0] is None or slot[0].numel() < work.size:
             slot[0] = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
         if self._work_dev is None or self._work_dev.numel() < work.size:
+            if self._last_use is not None:
+                self._last_use.synchronize()  # the old buffer is no longer read when it is freed
             self._work_dev = torch.empty(work.size, dtype=torch.int32, device=self.device)
+        elif self._last_use is not None:
+            st.wait_event(self._last_use)  # the previous batch's calls have read the descriptor
         slot[0][: work.size].copy_(torch.from_numpy(work))
-        self._work_dev[: work.size].copy_(slot[0][: work.size], non_blocking=True)
+        with torch.cuda.stream(st):
+            self._work_dev[: work.size].copy_(slot[0][: work.size], non_blocking=True)
         slot[1] = torch.cuda.Event()
-        slot[1].record()
+        slot[1].record(st)
+        self._upload = (slot[1], st)
         self.work_host = work
         if self._o_part is None or self._o_part.shape[0] < self.part_rows:
             self._o_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32,
@@ -111,14 +128,30 @@ class SplitKVAttention:
         return _k.splitkv_auto_kernel(self.Hq, self.Hkv, self.d, self.block_len, self.max_q_len, code)
 
     # device steps -----------------------------------------------------------
+    def _begin(self, stream):
+        """The stream of a device call, made to wait for the work upload if that ran elsewhere."""
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        ev, up = self._upload
+        if st != up:
+            st.wait_event(ev)
+        return st
+
+    def _end(self, st):
+        self._last_use = torch.cuda.Event()
+        self._last_use.record(st)
+
     def partial(self, q, k_pool, v_pool, block_table, scale, stream=None):
+        st = self._begin(stream)
         _k.splitkv_attn_partial(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
                                 self.total_q, self.max_q_len, self.block_len, scale, self.causal,
-                                self._o_part, self._lse_part, kernel=self.kernel, stream=stream)
+                                self._o_part, self._lse_part, kernel=self.kernel, stream=st)
+        self._end(st)
 
     def merge(self, out, lse, stream=None):
+        st = self._begin(stream)
         _k.splitkv_merge(self._o_part, self._lse_part, self._work_dev, self.B, self.total_q, out, lse,
-                         stream=stream)
+                         stream=st)
+        self._end(st)
 
     def backward(self, q, k_pool, v_pool, block_table, scale, out, lse, dout, stream=None):
         """Gradients of the forward pass that produced (out, lse) for upstream gradient dout.
@@ -127,6 +160,11 @@ class SplitKVAttention:
         written by every call and the slots without a key stay zero, so they are cleared only when
         the pool shape or the block table (storage or in-place version) changes."""
         dev = q.device
+        st = self._begin(stream)
+        with torch.cuda.stream(st):  # this call's buffers are allocated on the stream that uses them
+            return self._backward(q, k_pool, v_pool, block_table, scale, out, lse, dout, st, dev)
+
+    def _backward(self, q, k_pool, v_pool, block_table, scale, out, lse, dout, stream, dev):
         delta = torch.empty((self.total_q, self.Hq), dtype=torch.float32, device=dev)
         _k.splitkv_bwd_delta(out, dout, delta, stream=stream)
         dq_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32, device=dev)
@@ -140,15 +178,19 @@ class SplitKVAttention:
                                  delta, dq_part, dk, dv, stream=stream)
         dq = torch.empty((self.total_q, self.Hq, self.d), dtype=torch.float32, device=dev)
         _k.splitkv_dq_reduce(dq_part, self._work_dev, self.B, self.total_q, dq, stream=stream)
+        self._end(stream)
         return dq, dk, dv
 
     def fused_call(self, q, k_pool, v_pool, block_table, scale, out, lse, stream=None):
+        st = self._begin(stream)
         if self._tickets is None:
             n = _k.splitkv_ticket_count(self.B, self.Hq, self.Hkv, self.max_q_len)
-            self._tickets = torch.zeros(n, dtype=torch.int32, device=self.device)
+            with torch.cuda.stream(st):
+                self._tickets = torch.zeros(n, dtype=torch.int32, device=self.device)
         _k.splitkv_attn_fused(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
                               self.total_q, self.max_q_len, self.block_len, scale, self.causal, self._o_part,
-                              self._lse_part, self._tickets, out, lse, kernel=self.kernel, stream=stream)
+                              self._lse_part, self._tickets, out, lse, kernel=self.kernel, stream=st)
+        self._end(st)
 
     @property
     def tickets(self):

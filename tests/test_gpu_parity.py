@@ -224,3 +224,29 @@ def test_dcp_plan_through_the_kernels(name, beta, gamma):
     torch.cuda.synchronize()
     eo, el = max_errors(out, lse, *full_reference(inp))
     assert_close(w, eo, el, f"dcp {name}")
+
+
+def test_runner_on_a_side_stream():
+    """Plans uploaded on one stream and device calls on another: the runner orders the
+    work upload before the calls and the next upload after them."""
+    w = SMALL["shortq_small"]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, device="cuda")
+    side = torch.cuda.Stream()
+    o_ref, l_ref = full_reference(inp)
+    for plan_stream in (side, None):  # upload on the side stream, then on the current one
+        for _ in range(3):
+            run.plan(stream=plan_stream)
+            with torch.cuda.stream(side):
+                out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device="cuda")
+                lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device="cuda")
+            run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, stream=side)
+        side.synchronize()
+        eo, el = max_errors(out, lse, o_ref, l_ref)
+        assert_close(w, eo, el, f"side stream, plan on {'side' if plan_stream else 'current'}")
+    dq, dk, dv = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse,
+                              torch.ones_like(out), stream=side)
+    side.synchronize()
+    assert torch.isfinite(dq).all()
+    assert K.splitkv_device_status(clear=True) == 0
