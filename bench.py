@@ -175,7 +175,10 @@ def load_peaks():
 
 
 def workload_accounting(w, q_len, kv_len, block_cost, part_rows):
-    """Algorithmic flops and bytes of one pass (see the module docstring of DESIGN)."""
+    """Algorithmic flops and bytes of one pass: flops = 4 d Hq x (visible query-key pairs,
+    the sum of the block costs); K/V bytes = sum(kv_len) Hkv d x 2 tensors x element size,
+    each read once; Q bytes likewise; partial bytes = part_rows Hq (d + 1) x 4 (fp32 O_i and
+    L_i, written by the partial kernel and read by the merge)."""
     pairs = int(np.sum(block_cost))  # visible (query token, key) pairs, per query head
     flops = 4.0 * w.d * w.Hq * pairs
     kv_bytes = float(sum(kv_len)) * w.Hkv * w.d * 2 * w.elem_bytes
