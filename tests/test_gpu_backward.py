@@ -48,6 +48,37 @@ def test_backward_matches_oracle(name):
         assert err <= tol, f"{name} {nm}: max err {err:.3e} > {tol}"
 
 
+def test_backward_ragged_batch_with_empty_and_single_key_sequences():
+    """A sequence with no queries (no gradient anywhere), one with a single key, one over
+    several tiles and one short block, through the tensor-core backward."""
+    w = wl.custom("varlen", B=4, block_len=128, n_shards=5)
+    lens = ([0, 1, 130, 7], [5, 1, 400, 7])
+    inp, run, out, lse = run_cuda(w, lens=lens)
+    assert K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, K.SPLITKV_BF16) == K.KERNEL_TC
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dout = torch.randn(out.shape, generator=g, device="cuda", dtype=torch.float32).to(out.dtype)
+    dq, dk, dv = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+    torch.cuda.synchronize()
+    assert K.splitkv_device_status() == 0
+    args = (inp.q.cpu(), inp.k_pool.cpu(), inp.v_pool.cpu(), inp.block_table.cpu(), inp.q_len, inp.kv_len,
+            w.block_len, w.causal, w.scale)
+    o_ref, l_ref = oracle.attention(*args)
+    do64 = dout.cpu().double()
+    rdq, rdk, rdv = oracle.attention_backward(*args, do=do64, lse=l_ref, dlt=oracle.delta(o_ref, do64))
+    valid = torch.zeros(inp.k_pool.shape[:2], dtype=torch.bool)
+    table = inp.block_table.cpu()
+    for b, n in enumerate(inp.kv_len):
+        for j in range(-(-n // w.block_len)):
+            valid[int(table[b, j]), : min(w.block_len, n - j * w.block_len)] = True
+    for nm, got, ref in (("dq", dq.cpu().double(), rdq), ("dk", dk.cpu().double()[valid], rdk[valid]),
+                         ("dv", dv.cpu().double()[valid], rdv[valid])):
+        err = (got - ref).abs().max().item()
+        assert err <= TOL[w.dtype], f"{nm}: max err {err:.3e}"
+    # the sequence without queries has no gradient on its keys
+    b0 = [int(table[0, j]) for j in range(-(-inp.kv_len[0] // w.block_len))]
+    assert (dk[b0, : inp.kv_len[0]] == 0).all() and (dv[b0, : inp.kv_len[0]] == 0).all()
+
+
 def test_backward_is_deterministic_in_dk_dv_and_close_in_dq():
     w = SMALL["varlen_small"]
     inp, run, out, lse = run_cuda(w)
