@@ -1,7 +1,7 @@
 // Tensor-core backward of the split-KV attention for sm_103a: TMA + tcgen05 +
 // TMEM.  Same results as the CUDA-core backward in backward.cu (per-shard dK,
-// dV and partial dQ over the work items), for the shapes the forward's
-// tensor-core kernel takes: bf16, d = 128, block_len % 128 == 0, G | 128.
+// dV and partial dQ over the work items), for bf16, d = 128, block_len % 128 == 0
+// and G | 64 (a 64-row tile of the dK/dV kernel holds whole query tokens).
 //
 // The Split-KV card places the method in training (card intro) and states it
 // is exact ("All Facts").  With the merged forward's L and D = rowsum(dO * O),
