@@ -2,16 +2,22 @@
 
 A step is one pass of the whole path over one batch of resident synthetic
 input: block costs -> LPT plan -> work lists (host) -> work upload ->
-partial attention -> merge (device).  Default workload: batched decode
-(B=8, Hq=32, Hkv=8, d=128, one query per sequence over 32768 keys, bf16, paged
-block_len 256, 16 shards), whose metric is K/V read bandwidth.
+partial attention -> merge (device).  Default workload: the largest single-GPU
+shape (B=1, Hq=32, Hkv=8, d=128, 256 causal queries after a 1,048,576-token
+context, bf16, paged block_len 2048, 64 shards), bound by the bf16 tensor pipe:
+its value is TFLOP/s.  A workload bound by HBM (decode) reports GB/s of K/V read.
+The same run also times the decode, short-query and variable-length forward
+workloads and the short-query backward pass, each under ``per_workload``.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload largest]
                     [--impl ours|reference] [--kernel auto|simt|decode|tc]
+                    [--per-workload decode,shortq,varlen] [--per-backward shortq]
 
---gpus N > 1 runs under torchrun with one process per GPU; every rank solves
-its own copy of the workload (replicas; the path has no cross-GPU exchange on
-one device), value = all ranks' bytes / max-over-ranks time.
+--gpus N > 1 runs one process per GPU under torch.distributed.run (bench.py
+relaunches itself that way when started without WORLD_SIZE; a WORLD_SIZE that
+differs from N is an error).  Every rank solves its own copy of the workload
+(replicas; the path has no cross-GPU exchange on one device): value = all
+ranks' work / max-over-ranks time.
 --impl reference times the fp64 CPU oracle on the host cores instead.
 """
 
@@ -40,11 +46,15 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="largest")
+    ap.add_argument("--per-workload", default="decode,shortq,varlen",
+                    help="forward workloads also timed in the same run (comma list, '' for none)")
+    ap.add_argument("--per-backward", default="shortq",
+                    help="workloads whose backward pass is also timed in the same run ('' for none)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "decode", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--fused", action="store_true",
                     help="splitkv_attn_fused (one launch with the decode kernel) instead of partial + merge")
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
@@ -174,6 +184,15 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def unit_pairs(q_len, kv_len, causal):
+    """Visible (query token, key) pairs of one sequence: q_len x kv_len without a mask; with
+    the causal tail token t sees kv_len - q_len + t + 1 keys."""
+    q_len, kv_len = int(q_len), int(kv_len)
+    if not causal:
+        return q_len * kv_len
+    return q_len * (kv_len - q_len) + q_len * (q_len + 1) // 2
+
+
 def workload_accounting(w, q_len, kv_len, block_cost, part_rows):
     """Algorithmic flops and bytes of one pass: flops = 4 d Hq x (visible query-key pairs,
     the sum of the block costs); K/V bytes = sum(kv_len) Hkv d x 2 tensors x element size,
@@ -220,28 +239,48 @@ def dcp_model(w):
 # -------------------------------------------------------------- our arm
 
 
-def run_ours(args, dctx):
+def _binding(w, acc, peaks):
+    """The roofline that binds the partial kernel: HBM when its algorithmic intensity is
+    below the ridge (peak flops / peak bytes), the bf16 tensor pipe above it."""
+    return "hbm" if acc["flops"] / acc["partial_bytes"] < 1e3 * peaks["bf16_tflops"] / peaks["hbm_gbs"] else "tensor"
+
+
+def _timed_steps(torch, n, step, stream, sampler):
+    """n steps, each bracketed by events; returns (total s, mean per-step event deltas, clocks)."""
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n)]
+    if sampler is not None:
+        sampler.start()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(n):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
+    return t0.elapsed_time(t1) / 1e3, evs, clocks
+
+
+def measure_forward(args, dctx, name, dev, headline=False):
+    """Times the forward path of one workload; returns (bench fields, objects for e2e / cpu)."""
     import torch
 
     from context_long_attention_lpt_gb300 import splitkv as K
     from context_long_attention_lpt_gb300 import workloads as wl
     from context_long_attention_lpt_gb300.runner import SplitKVAttention
 
-    dctx.init("nccl")
-    dev = dctx.local_rank
-    torch.cuda.set_device(dev)
-    K.lib()
-    w = wl.WORKLOADS[args.workload]
-    if args.context:
+    w = wl.WORKLOADS[name]
+    if args.context and headline:
         w = wl.custom(w, context=args.context)
     kernel = {"auto": K.KERNEL_AUTO, "simt": K.KERNEL_SIMT, "decode": K.KERNEL_DECODE,
-              "tc": K.KERNEL_TC}[args.kernel]
+              "tc": K.KERNEL_TC}[args.kernel if headline else "auto"]
     inp = wl.make_inputs(w, device=f"cuda:{dev}")
     alpha, beta, gamma = dcp_model(w)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
                            inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
                            planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma)
-    fused_one_launch = run.fused and run.kernel_used() == K.KERNEL_DECODE
+    fused_one_launch = run.fused and run.fuses_in_one_launch()
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
     acc = workload_accounting(w, inp.q_len, inp.kv_len, run.block_cost, run.part_rows)
@@ -255,6 +294,7 @@ def run_ours(args, dctx):
             run.fused_call(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse)
             if ev is not None:
                 ev[1].record(stream)
+                ev[2].record(stream)
             return
         run.partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
         if ev is not None:
@@ -266,135 +306,182 @@ def run_ours(args, dctx):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if args.backward:
-        return run_backward(args, dctx, w, inp, run, out, lse, acc)
-
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     sampler = ClockSampler(gpu_nvsmi_id(torch, dev), os.path.join(ROOT, f".bench_clocks_{dctx.rank}.csv"))
-    sampler.start()
     dctx.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     host0 = time.perf_counter()
-    t0.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
+    local_s, evs, clocks = _timed_steps(torch, args.steps, step, stream, sampler)
     host_s = time.perf_counter() - host0
     dctx.barrier()
-    clocks = sampler.stop()
     try:
         os.remove(sampler.path)
     except OSError:
         pass
-    local_s = t0.elapsed_time(t1) / 1e3
-    partial_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)  # the dominant kernel's launch
+    kernel_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)  # the dominant kernel's launch
     merge_ms = None if run.fused else sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
-    t_max, units = aggregate(dctx, local_s, acc["kv_bytes"] * args.steps, device=f"cuda:{dev}")
-    ms_per_step = 1e3 * t_max / args.steps
-
-    # planner time alone (host), for the report
-    tp = time.perf_counter()
-    for _ in range(20):
-        K.splitkv_plan(K.splitkv_block_costs(run._q_len_np, run._kv_len_np, w.block_len, w.causal),
-                       w.n_shards)
-    planner_us = (time.perf_counter() - tp) / 20 * 1e6
-
-    # end to end: host inputs -> device, the path, result -> host, every step
-    e2e = None
-    if args.e2e_steps > 0:
-        e2e = run_e2e(args, w, inp, run, dev, acc)
 
     peaks, peak_src = load_peaks()
     kname = K.KERNEL_NAMES[run.kernel_used()] + ("_fused" if fused_one_launch else "")
     if fused_one_launch:  # the same launch also reads the partials back and writes the output
         acc["partial_bytes"] += acc["part_bytes"] + float(run.total_q) * w.Hq * (w.d * w.elem_bytes + 4)
-    hbm_bound = (acc["flops"] / acc["partial_bytes"]) < 1e3 * peaks["bf16_tflops"] / peaks["hbm_gbs"]
-    if hbm_bound:
-        achieved = acc["partial_bytes"] / (partial_ms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak}
+    bound = _binding(w, acc, peaks)
+    if bound == "hbm":
+        achieved = acc["partial_bytes"] / (kernel_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+        units_local, unit, scale = acc["kv_bytes"] * args.steps, "GB/s", 1e9
     else:
-        achieved = acc["flops"] / (partial_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+        achieved = acc["flops"] / (kernel_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+        units_local, unit, scale = acc["flops"] * args.steps, "TFLOP/s", 1e12
     roof.update({"traffic": traffic_for(f"partial_{kname}", w.name), "kernel": f"partial_{kname}",
-                 "kernel_ms": partial_ms, "merge_ms": merge_ms, "peak_source": peak_src,
-                 "algorithmic_per_launch": acc["partial_bytes"] if hbm_bound else acc["flops"]})
-
-    value = units / t_max / 1e9  # GB/s of K/V read, all ranks
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dctx.world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "tflops": acc["flops"] * args.steps * dctx.world / t_max / 1e12,
-        "config": {"workload": w.name, "shape": w.description, "kernel": kname,
-                   "n_items": run.n_items, "lpt_imbalance": run.imbalance, "planner": args.planner,
-                   "shards_used": run.n_shards_used, "part_rows": run.part_rows,
-                   "planner_us": planner_us, "host_s": host_s,
-                   "l2": f"inputs larger than L2 (K/V {acc['kv_bytes'] / 1e9:.2f} GB vs L2 "
-                         f"{L2_BYTES / 1e6:.0f} MB); no flush"
-                         if acc["kv_bytes"] > L2_BYTES else "inputs smaller than L2; not flushed",
-                   "parallelism": f"replicas x{dctx.world}"},
-        "roofline": roof,
+                 "kernel_ms": kernel_ms, "merge_ms": merge_ms, "peak_source": peak_src,
+                 "algorithmic_per_launch": acc["partial_bytes"] if bound == "hbm" else acc["flops"]})
+    t_max, units = aggregate(dctx, local_s, units_local, device=f"cuda:{dev}")
+    _, kv_all = aggregate(dctx, local_s, acc["kv_bytes"] * args.steps, device=f"cuda:{dev}")
+    _, fl_all = aggregate(dctx, local_s, acc["flops"] * args.steps, device=f"cuda:{dev}")
+    fields = {
+        "value": units / t_max / scale, "unit": unit, "ms_per_step": 1e3 * t_max / args.steps,
+        "steps": args.steps, "kv_gbs": kv_all / t_max / 1e9, "tflops": fl_all / t_max / 1e12,
+        "shape": w.description, "kernel": kname, "n_items": run.n_items, "lpt_imbalance": run.imbalance,
+        "planner": args.planner, "shards_used": run.n_shards_used, "part_rows": run.part_rows,
+        "host_s": host_s, "roofline": roof, "clocks": clocks,
         "gpu_launches": (1 if fused_one_launch else 2) * args.steps,
-        "clocks": clocks,
-        "e2e": e2e,
+        "l2": (f"inputs larger than L2 (K/V {acc['kv_bytes'] / 1e9:.2f} GB vs L2 {L2_BYTES / 1e6:.0f} MB); "
+               "no flush") if acc["kv_bytes"] > L2_BYTES else "inputs smaller than L2; not flushed",
     }
-    if dctx.rank == 0 and dctx.world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
-    if dctx.rank == 0:
-        print(json.dumps(line), flush=True)
-    dctx.finish()
+    return fields, (w, inp, run, acc, bound)
 
 
-def run_backward(args, dctx, w, inp, run, out, lse, acc):
-    """Backward pass of the same plan: the forward output is computed once (untimed), then
-    K timed backward steps.  Algorithmic flops = 2.5 x forward (QK^T recompute, dP, dV, dQ, dK)."""
+def measure_backward(args, dctx, name, dev):
+    """Times the backward pass of one workload (delta, per-shard dK/dV + partial dQ, dQ
+    reduction) over its LPT plan; the forward output is computed once, untimed."""
+    import torch
+
+    from context_long_attention_lpt_gb300 import splitkv as K
+    from context_long_attention_lpt_gb300 import workloads as wl
+    from context_long_attention_lpt_gb300.runner import SplitKVAttention
+
+    w = wl.WORKLOADS[name]
+    if args.context and args.backward:
+        w = wl.custom(w, context=args.context)
+    inp = wl.make_inputs(w, device=f"cuda:{dev}")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, device=f"cuda:{dev}")
+    out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    acc = workload_accounting(w, inp.q_len, inp.kv_len, run.block_cost, run.part_rows)
+    g = torch.Generator(device=out.device).manual_seed(0)
+    dout = torch.randn(out.shape, generator=g, device=out.device, dtype=torch.float32).to(out.dtype)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+
+    for _ in range(max(2, min(args.warmup, 5))):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    sampler = ClockSampler(gpu_nvsmi_id(torch, dev), os.path.join(ROOT, f".bench_clocks_{dctx.rank}.csv"))
+    dctx.barrier()
+    local_s, _, clocks = _timed_steps(torch, n, step, stream, sampler)
+    dctx.barrier()
+    try:
+        os.remove(sampler.path)
+    except OSError:
+        pass
+    flops = 2.5 * acc["flops"]
+    t_max, units = aggregate(dctx, local_s, flops * n, device=f"cuda:{dev}")
+    s = t_max / n
+    peaks, src = load_peaks()
+    code = K.SPLITKV_BF16 if w.dtype == "bf16" else K.SPLITKV_F32
+    tc = K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, code) == K.KERNEL_TC
+    achieved = flops / (local_s / n) / 1e12
+    if tc:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": src,
+                "note": "whole backward step: delta, dQ and dK/dV tensor-core kernels, dQ reduction"}
+    else:
+        roof = {"bound": "fp32_fma", "achieved": achieved, "unit": "TFLOP/s",
+                "note": "CUDA-core kernel: bf16 inputs, fp32 FMA arithmetic"}
+    return {"value": units / t_max / 1e12, "unit": "TFLOP/s", "ms_per_step": 1e3 * s, "steps": n,
+            "shape": w.description, "kernel": "backward_tcgen05" if tc else "backward_simt",
+            "lpt_imbalance": run.imbalance, "roofline": roof, "clocks": clocks,
+            "gpu_launches": (4 if tc else 5) * n,
+            "accounting": "flops = 2.5 x forward (QK^T recomputed, dP, dV, dQ, dK)"}
+
+
+def run_ours(args, dctx):
     import torch
 
     from context_long_attention_lpt_gb300 import splitkv as K
 
-    g = torch.Generator(device=out.device).manual_seed(0)
-    dout = torch.randn(out.shape, generator=g, device=out.device, dtype=torch.float32).to(out.dtype)
-    for _ in range(2):
-        run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
-    t1.record()
-    torch.cuda.synchronize()
-    s = t0.elapsed_time(t1) / 1e3 / args.steps
-    flops = 2.5 * acc["flops"]
-    peaks, src = load_peaks()
-    code = K.SPLITKV_BF16 if w.dtype == "bf16" else K.SPLITKV_F32
-    tc = K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, code) == K.KERNEL_TC
-    kname = "backward_tcgen05" if tc else "backward_simt"
-    if tc:
-        roof = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": flops / s / 1e12 / peaks["bf16_tflops"], "peak_source": src,
-                "note": "dQ and dK/dV tensor-core kernels plus delta and dQ reduction, whole backward step"}
-    else:
-        roof = {"bound": "fp32_fma", "achieved": flops / s / 1e12, "unit": "TFLOP/s",
-                "note": "CUDA-core kernel: bf16 inputs, fp32 FMA arithmetic"}
-    line = {"metric": METRIC + " (backward pass)", "value": flops / s / 1e12, "unit": "TFLOP/s",
-            "n_gpus": dctx.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s,
-            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "shape": w.description, "kernel": kname},
-            "roofline": roof}
+    dctx.init("nccl")
+    dev = dctx.local_rank
+    torch.cuda.set_device(dev)
+    K.lib()
+    if args.backward:
+        f = measure_backward(args, dctx, args.workload, dev)
+        line = {"metric": METRIC + " (backward pass)", "value": f["value"], "unit": f["unit"],
+                "n_gpus": dctx.world, "steps": f["steps"], "warmup": args.warmup, "ms_per_step": f["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": args.workload, "shape": f["shape"],
+                                                "kernel": f["kernel"], "parallelism": f"replicas x{dctx.world}"},
+                "roofline": f["roofline"], "clocks": f["clocks"], "gpu_launches": f["gpu_launches"]}
+        if dctx.rank == 0:
+            print(json.dumps(line), flush=True)
+        dctx.finish()
+        return
+
+    f, (w, inp, run, acc, bound) = measure_forward(args, dctx, args.workload, dev, headline=True)
+    # planner time alone (host), for the report
+    tp = time.perf_counter()
+    for _ in range(20):
+        K.splitkv_plan(K.splitkv_block_costs(run._q_len_np, run._kv_len_np, w.block_len, w.causal), w.n_shards)
+    planner_us = (time.perf_counter() - tp) / 20 * 1e6
+    # end to end: host inputs -> device, the path, result -> host, every step
+    e2e = run_e2e(args, w, inp, run, dev, acc, bound) if args.e2e_steps > 0 else None
+    cpu = None
+    if dctx.rank == 0 and dctx.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_seconds, bound)
+    del inp, run
+    torch.cuda.empty_cache()
+
+    per = {}
+    for name in [x for x in args.per_workload.split(",") if x and x != args.workload]:
+        pf, objs = measure_forward(args, dctx, name, dev)
+        del objs
+        torch.cuda.empty_cache()
+        per[name] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "steps", "kv_gbs", "tflops", "shape",
+                                        "kernel", "n_items", "lpt_imbalance", "shards_used", "part_rows",
+                                        "roofline", "clocks", "gpu_launches", "l2")}
+    for name in [x for x in args.per_backward.split(",") if x]:
+        per[f"backward/{name}"] = measure_backward(args, dctx, name, dev)
+        torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": f["value"], "unit": f["unit"], "n_gpus": dctx.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": f["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "kv_gbs": f["kv_gbs"], "tflops": f["tflops"],
+        "config": {"workload": w.name, "shape": f["shape"], "kernel": f["kernel"], "n_items": f["n_items"],
+                   "lpt_imbalance": f["lpt_imbalance"], "planner": f["planner"], "shards_used": f["shards_used"],
+                   "part_rows": f["part_rows"], "planner_us": planner_us, "host_s": f["host_s"], "l2": f["l2"],
+                   "parallelism": f"replicas x{dctx.world}"},
+        "roofline": f["roofline"],
+        "gpu_launches": f["gpu_launches"],
+        "clocks": f["clocks"],
+        "e2e": e2e,
+        "per_workload": per,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if dctx.rank == 0:
         print(json.dumps(line), flush=True)
     dctx.finish()
 
 
-def run_e2e(args, w, inp, run, dev, acc):
+def run_e2e(args, w, inp, run, dev, acc, bound):
     import torch
 
     d = f"cuda:{dev}"
@@ -426,8 +513,12 @@ def run_e2e(args, w, inp, run, dev, acc):
     s = t0.elapsed_time(t1) / 1e3
     h2d += run.work_host.size * 4
     del dbuf
-    return {"value": acc["kv_bytes"] * n / s / 1e9, "unit": "GB/s", "ms_per_step": 1e3 * s / n,
-            "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    if bound == "hbm":
+        value, unit = acc["kv_bytes"] * n / s / 1e9, "GB/s"
+    else:
+        value, unit = acc["flops"] * n / s / 1e12, "TFLOP/s"
+    return {"value": value, "unit": unit, "ms_per_step": 1e3 * s / n, "steps": n,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
 # ------------------------------------------------------- oracle on the host
@@ -437,7 +528,8 @@ def _oracle_unit(w, inp_cpu, b, kvh, n_keys=None):
     """The oracle's unsharded attention for sequence b, K/V head kvh (its G query heads).
 
     ``n_keys`` truncates the sequence to its first n_keys keys (a bounded sample;
-    the queries keep their place at the end of the truncated sequence)."""
+    the queries keep their place at the end of the truncated sequence).  Returns the
+    (K/V bytes, flops) of the sample."""
     import oracle
 
     cu = int(sum(inp_cpu["q_len"][:b]))
@@ -449,33 +541,49 @@ def _oracle_unit(w, inp_cpu, b, kvh, n_keys=None):
     vp = inp_cpu["v_pool"][:, :, kvh: kvh + 1]
     table = inp_cpu["block_table"][b: b + 1]
     oracle.attention(q, kp, vp, table, [lq], [kv], w.block_len, w.causal, w.scale)
-    return kv
+    return float(kv) * w.d * 2 * w.elem_bytes, 4.0 * w.d * g * unit_pairs(lq, kv, w.causal)
 
 
-def _unit_bytes(w, n_keys):
-    return float(n_keys) * w.d * 2 * w.elem_bytes
+def _pick(bound, nbytes, flops, seconds):
+    return (nbytes / seconds / 1e9, "GB/s") if bound == "hbm" else (flops / seconds / 1e12, "TFLOP/s")
 
 
-def cpu_baseline(w, inp, seconds):
-    """Times the fp64 oracle as it stands on the host cores over a bounded sample."""
+def _sample_keys(w, cpu, budget_s):
+    """Keys per (sequence, K/V head) unit so that one unit of the oracle takes about budget_s."""
+    b0 = 0
+    probe = max(w.block_len, min(cpu["kv_len"][b0], 8192))
+    t0 = time.perf_counter()
+    _oracle_unit(w, cpu, b0, 0, n_keys=probe)
+    per_key = max((time.perf_counter() - t0) / probe, 1e-9)
+    n = int(budget_s / per_key)
+    return max(w.block_len, (n // w.block_len) * w.block_len)
+
+
+def cpu_baseline(w, inp, seconds, bound):
+    """Times the fp64 oracle as it stands on the host cores over a bounded sample: the
+    workload's (sequence, K/V head) units in order, each truncated to at most n_keys keys,
+    until about ``seconds`` have passed."""
     import torch
 
     torch.set_num_threads(os.cpu_count() or 1)
     cpu = {"q": inp.q.cpu(), "k_pool": inp.k_pool.cpu(), "v_pool": inp.v_pool.cpu(),
            "block_table": inp.block_table.cpu(), "q_len": inp.q_len, "kv_len": inp.kv_len}
     units = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    n_keys = _sample_keys(w, cpu, seconds / 6)
     t0 = time.perf_counter()
-    done, nbytes = 0, 0.0
+    done, nbytes, flops = 0, 0.0, 0.0
     for b, h in units:
-        nbytes += _unit_bytes(w, _oracle_unit(w, cpu, b, h))
+        nb, fl = _oracle_unit(w, cpu, b, h, n_keys=n_keys)
+        nbytes += nb
+        flops += fl
         done += 1
         if time.perf_counter() - t0 > seconds:
             break
     s = time.perf_counter() - t0
-    return {"value": nbytes / s / 1e9, "unit": "GB/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "seconds": s,
-            "sample": f"{done} of {len(units)} (sequence, K/V head) units of the workload, "
-                      f"fp64 unsharded attention over their full context"}
+    value, unit = _pick(bound, nbytes, flops, s)
+    return {"value": value, "unit": unit, "cores": torch.get_num_threads(), "kind": "oracle", "seconds": s,
+            "sample": f"{done} of {len(units)} (sequence, K/V head) units of the workload, each truncated to "
+                      f"its first {n_keys} keys (queries at the end), fp64 unsharded attention"}
 
 
 def run_reference(args, dctx):
@@ -492,37 +600,66 @@ def run_reference(args, dctx):
     cpu = {"q": inp.q, "k_pool": inp.k_pool, "v_pool": inp.v_pool, "block_table": inp.block_table,
            "q_len": inp.q_len, "kv_len": inp.kv_len}
     units = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
-    # size each step (keys of one (sequence, K/V head) unit) so the whole run fits the budget
-    t0 = time.perf_counter()
-    full = _oracle_unit(w, cpu, *units[0])
-    per_key = (time.perf_counter() - t0) / full
+    peaks, _ = load_peaks()
+    q_len, kv_len = inp.q_len, inp.kv_len
+    flops_all = sum(4.0 * w.d * w.Hq * unit_pairs(a, b, w.causal) for a, b in zip(q_len, kv_len))
+    kv_all = float(sum(kv_len)) * w.Hkv * w.d * 2 * w.elem_bytes
+    bound = "hbm" if flops_all / kv_all < 1e3 * peaks["bf16_tflops"] / peaks["hbm_gbs"] else "tensor"
+    # size each step (one truncated (sequence, K/V head) unit) so the whole run fits the budget
     budget = 150.0
-    n_keys = int(budget / (args.steps + args.warmup) / per_key)
-    n_keys = max(w.block_len, min(full, (n_keys // w.block_len) * w.block_len))
+    n_keys = _sample_keys(w, cpu, budget / (args.steps + args.warmup))
     for i in range(args.warmup):
         _oracle_unit(w, cpu, *units[i % len(units)], n_keys=n_keys)
     t0 = time.perf_counter()
-    nbytes = 0.0
+    nbytes, flops = 0.0, 0.0
     for i in range(args.steps):
         b, h = units[i % len(units)]
-        nbytes += _unit_bytes(w, _oracle_unit(w, cpu, b, h, n_keys=n_keys))
+        nb, fl = _oracle_unit(w, cpu, b, h, n_keys=n_keys)
+        nbytes += nb
+        flops += fl
     s = time.perf_counter() - t0
-    value = nbytes / s / 1e9
+    value, unit = _pick(bound, nbytes, flops, s)
     sample = (f"per step one (sequence, K/V head) unit of the workload truncated to its first {n_keys} "
               f"keys, fp64 unsharded attention")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dctx.world,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": dctx.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "shape": w.description},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "kind": "oracle",
                              "cores": torch.get_num_threads(), "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
 
+def relaunch_or_check(args, argv):
+    """--gpus N > 1 without WORLD_SIZE: run N ranks under torch.distributed.run and return
+    their exit code.  WORLD_SIZE set but different from N: an error.  Otherwise None."""
+    world = os.environ.get("WORLD_SIZE")
+    if world is None:
+        if args.gpus <= 1:
+            return None
+        import socket
+
+        with socket.socket() as s:
+            s.bind(("127.0.0.1", 0))
+            port = s.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + list(argv)
+        return subprocess.call(cmd)
+    if int(world) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one rank per GPU "
+              f"(torch.distributed.run --nproc-per-node {args.gpus})", file=sys.stderr)
+        return 2
+    return None
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     args = parse_args(argv)
+    rc = relaunch_or_check(args, argv)
+    if rc is not None:
+        sys.exit(rc)
     dctx = Dist()
     if args.impl == "reference":
         run_reference(args, dctx)

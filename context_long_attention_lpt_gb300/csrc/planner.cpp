@@ -189,6 +189,24 @@ extern "C" int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t
   return SPLITKV_OK;
 }
 
+extern "C" int splitkv_imbalance(const int64_t* shard_load, int32_t n_shards, double* rate) {
+  if (!shard_load || !rate || n_shards <= 0)
+    return fail(SPLITKV_ERR_INVALID, "splitkv_imbalance: need the loads of n_shards > 0 shards");
+  int64_t total = 0, mx = 0;
+  for (int32_t s = 0; s < n_shards; ++s) {
+    if (shard_load[s] < 0) return fail(SPLITKV_ERR_INVALID, "negative load on shard %d", s);
+    if (shard_load[s] > (int64_t(1) << 53) - 1 - total)
+      return fail(SPLITKV_ERR_INVALID, "splitkv_imbalance: loads sum past 2^53");
+    total += shard_load[s];
+    mx = std::max(mx, shard_load[s]);
+  }
+  // max / mean - 1 with mean = total / n; total < 2^53, so both conversions are exact
+  const double mean = static_cast<double>(total) / static_cast<double>(n_shards);
+  *rate = total == 0 ? 0.0 : static_cast<double>(mx) / mean - 1.0;
+  splitkv::clear_error();
+  return SPLITKV_OK;
+}
+
 extern "C" int64_t splitkv_work_words(int64_t n_blocks, int32_t B) {
   if (n_blocks < 0 || B <= 0) return fail(SPLITKV_ERR_INVALID, "splitkv_work_words: bad arguments");
   return splitkv::kHeaderWords + splitkv::kSeqWords * (static_cast<int64_t>(B) + 1) +

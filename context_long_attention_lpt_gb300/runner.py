@@ -105,9 +105,8 @@ class SplitKVAttention:
 
     @property
     def imbalance(self):
-        load = self.shard_load[: self.n_shards_used]
-        mean = load.sum() / len(load)
-        return float(load.max() / mean - 1.0) if mean > 0 else 0.0
+        """max / mean - 1 of the shard loads of the current plan (from the library)."""
+        return _k.splitkv_imbalance(self.shard_load[: self.n_shards_used])
 
     @property
     def o_part(self):
@@ -126,6 +125,10 @@ class SplitKVAttention:
             return self.kernel
         code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
         return _k.splitkv_auto_kernel(self.Hq, self.Hkv, self.d, self.block_len, self.max_q_len, code)
+
+    def fuses_in_one_launch(self):
+        """Whether splitkv_attn_fused merges inside the partial kernel's launch for this shape."""
+        return self.kernel_used() == _k.KERNEL_DECODE
 
     # device steps -----------------------------------------------------------
     def _begin(self, stream):

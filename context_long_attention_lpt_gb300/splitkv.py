@@ -27,6 +27,7 @@ _SIGNATURES = {
     "splitkv_num_blocks": (_i64, [_p, _i32, _i32]),
     "splitkv_block_costs": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _i64]),
     "splitkv_plan": (ctypes.c_int, [_p, _i64, _i32, _p, _p]),
+    "splitkv_imbalance": (ctypes.c_int, [_p, _i32, _p]),
     "splitkv_plan_dcp": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, ctypes.c_double, ctypes.c_double,
                                         ctypes.c_double, _p, _i64, _p, _p, _p]),
     "splitkv_work_words": (_i64, [_i64, _i32]),
@@ -125,6 +126,14 @@ def splitkv_plan(block_cost, n_shards):
     load = np.zeros(n_shards, dtype=np.int64)
     _check("splitkv_plan", lib().splitkv_plan(_ptr(c), len(c), n_shards, _ptr(sob), _ptr(load)))
     return sob, load
+
+
+def splitkv_imbalance(shard_load):
+    """max / mean - 1 of the shard loads, computed by the library."""
+    load = _np(shard_load, np.int64)
+    r = ctypes.c_double(0.0)
+    _check("splitkv_imbalance", lib().splitkv_imbalance(_ptr(load), len(load), ctypes.byref(r)))
+    return r.value
 
 
 def splitkv_plan_dcp(q_len, kv_len, block_len, causal, max_shards, alpha, beta, gamma=0.0):

@@ -81,6 +81,13 @@ int splitkv_block_costs(const int32_t* q_len, const int32_t* kv_len, int32_t B,
 int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t n_shards,
                  int32_t* shard_of_block, int64_t* shard_load);
 
+/* Load imbalance of a plan (Split-KV card, "Timeline" / "All Facts": the LPT
+ * allocation keeps it below 1%).  The card gives no definition; the rate here is
+ * max load / mean load - 1, with mean = (sum of the loads) / n_shards, in IEEE
+ * double (0 when every load is 0).  In (host): shard_load[n_shards], each >= 0,
+ * summing below 2^53 (so the sum converts to double exactly).  Out: *rate. */
+int splitkv_imbalance(const int64_t* shard_load, int32_t n_shards, double* rate);
+
 /* Step 2, alternative planner: split selection that models the completion of
  * attention together with the reduction that depends on it (after the LiquidCP
  * abstract, PaperTrail: its MegaDCP selects history-KV splits this way; the
@@ -207,9 +214,14 @@ int splitkv_merge(const float* o_part, const float* lse_part, int64_t part_rows,
  * which every GPU that loads the library holds until the process exits.
  *   - Needs 4*words + 4*part_rows*Hq*(d+1) bytes (each part rounded up to 256);
  *     larger problems are rejected with SPLITKV_ERR_CAPACITY before any work.
+ *   - work_host is checked on the host before any work: its n_items, B,
+ *     total_q and max_q_len must equal the arguments, its offsets must lie
+ *     inside work_words, and part_rows must equal the rows its items address
+ *     (largest part_row + q_len); otherwise SPLITKV_ERR_INVALID.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *     device, with that device current; again after that device's context was
+ *     destroyed and created anew); make that first call before any stream
+ *     capture.
  *   - Every call shares the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero (each partial row read is written
  *     first).  Calls whose GPU work overlaps - on different streams, or from

@@ -52,13 +52,19 @@ def lpt_assign(costs, n_shards):
     load = [0] * n_shards
     shard_of_block = [-1] * len(costs)
     for g in order:
-        best = 0
-        for s in range(1, n_shards):
-            if load[s] < load[best]:
-                best = s
+        best = least_loaded(load)
         shard_of_block[g] = best
         load[best] += int(costs[g])
     return shard_of_block, load
+
+
+def least_loaded(load):
+    """Index of the smallest load; equal loads go to the lower shard id."""
+    best = 0
+    for s in range(1, len(load)):
+        if load[s] < load[best]:
+            best = s
+    return best
 
 
 def imbalance(load):

@@ -65,3 +65,24 @@ def test_committed_traffic_entries_are_well_formed(key):
         e = json.load(f)[key]
     assert os.path.exists(os.path.join(bench.ROOT, e["source"]))
     assert len(e["sha256"]) == 64 and e["bytes_per_launch"] > 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "shortq", "varlen", "largest"])
+def test_unit_pairs_equal_the_oracle_block_costs(name):
+    """The closed form the CPU baseline and the reference arm count flops with equals the
+    oracle's block costs summed over each sequence."""
+    w = wl.WORKLOADS[name]
+    q_len, kv_len = wl.lengths(w)
+    for lq, lk in zip(q_len, kv_len):
+        assert bench.unit_pairs(lq, lk, w.causal) == sum(oracle.block_costs([lq], [lk], w.block_len, w.causal))
+    assert bench.unit_pairs(3, 10, True) == 8 + 9 + 10
+    assert bench.unit_pairs(3, 10, False) == 30
+
+
+def test_reference_arm_line_on_the_tiny_workload(capsys):
+    """The reference arm (the oracle on the host) prints one JSON line with the contract's keys."""
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] in ("GB/s", "TFLOP/s")
+    assert line["config"]["workload"] == "tiny" and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

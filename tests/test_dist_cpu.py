@@ -49,3 +49,15 @@ def test_single_process_aggregate_is_identity():
 
     d = bench.Dist()
     assert bench.aggregate(d, 3.5, 7) == (3.5, 7)
+
+
+def test_bench_refuses_a_world_size_other_than_gpus():
+    """--gpus N under a launcher that started a different number of ranks is an error."""
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "WORLD_SIZE" in r.stderr

@@ -13,26 +13,11 @@ import oracle
 from context_long_attention_lpt_gb300 import splitkv as K
 from context_long_attention_lpt_gb300 import workloads as wl
 from context_long_attention_lpt_gb300.runner import SplitKVAttention
-from tests.parity_helpers import (TOL_L, TOL_O, assert_close, compare_rows, full_reference,
+from tests.parity_helpers import (SMALL, TOL_L, TOL_O, assert_close, compare_rows, full_reference,  # noqa: F401
                                   max_errors, run_cuda, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
-SMALL = {
-    "tiny": wl.WORKLOADS["tiny"],
-    "decode_small": wl.custom("decode", B=3, context=3000, n_shards=5),
-    "decode_gqa8": wl.custom("decode", B=2, Hq=64, Hkv=8, context=1500, n_shards=4),
-    "shortq_small": wl.custom("shortq", q_len=77, context=2500, block_len=256, n_shards=7),
-    "varlen_small": wl.custom("varlen", B=4, ctx_range=(100, 3000), q_range=(1, 300), block_len=128,
-                              n_shards=6),
-    "largest_small": wl.custom("largest", q_len=64, context=5000, block_len=512, n_shards=3),
-    "noncausal_multi_q": wl.custom("shortq", causal=False, q_len=9, context=1000, block_len=128,
-                                   n_shards=4),
-    "bf16_d64": wl.custom("shortq", d=64, q_len=20, context=900, block_len=128, n_shards=3),
-    # causal queries longer than the context, one block per shard: the first query rows see
-    # none of the last blocks, so many (item, head, row tile) units have no key tile at all
-    "causal_empty_units": wl.custom("shortq", q_len=600, context=100, block_len=128, n_shards=6),
-}
 
 
 @pytest.fixture(scope="module", autouse=True)

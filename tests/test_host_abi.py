@@ -137,12 +137,31 @@ def test_work_lists_cover_the_plan(k, name):
 
 
 def test_imbalance_on_workloads(k):
-    """Report max/mean - 1 of the LPT loads; the hand-derived values are pinned in test_oracle."""
+    """The library's max/mean - 1 of the LPT loads equals the oracle's bit for bit; the
+    hand-derived values for the workloads are pinned in test_oracle."""
     for name in wl.WORKLOADS:
         w = wl.WORKLOADS[name]
         q, kv = wl.lengths(w)
         _, load = k.splitkv_plan(k.splitkv_block_costs(q, kv, w.block_len, w.causal), w.n_shards)
-        assert abs((load.max() / load.mean() - 1) - oracle.imbalance(load.tolist())) < 1e-12
+        assert k.splitkv_imbalance(load) == oracle.imbalance(load.tolist())
+
+
+def test_imbalance_fuzz_and_edges(k):
+    rng = np.random.default_rng(17)
+    for _ in range(2000):
+        n = int(rng.integers(1, 70))
+        hi = int(rng.choice([3, 1000, 1 << 40]))
+        load = rng.integers(0, hi, size=n).astype(np.int64)
+        assert k.splitkv_imbalance(load) == oracle.imbalance(load.tolist())
+    assert k.splitkv_imbalance(np.zeros(5, dtype=np.int64)) == 0.0
+    assert k.splitkv_imbalance(np.array([7, 7, 7], dtype=np.int64)) == 0.0
+    assert k.splitkv_imbalance(np.array([3, 1], dtype=np.int64)) == 0.5
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_imbalance(np.array([1, -1], dtype=np.int64))
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_imbalance(np.array([1 << 53, 1], dtype=np.int64))
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_imbalance(np.zeros(0, dtype=np.int64))
 
 
 def test_errors_are_statuses_not_crashes(k):

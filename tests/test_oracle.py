@@ -353,19 +353,20 @@ def test_planted_unweighted_merge_is_caught():
     assert (bad - o_ref).abs().max() > 1e-3
 
 
-def test_planted_reversed_tie_break_is_caught(golden):
-    c = golden["lpt_ties"][0]
+def test_planted_reversed_tie_break_is_caught(golden, monkeypatch):
+    """oracle.lpt_assign with its least-loaded choice sending equal loads to the HIGHEST shard
+    id no longer reproduces the hand-worked tie cases."""
+    from oracle import lpt as olpt
 
-    def lpt_high_tie(costs, S):
-        order = sorted(range(len(costs)), key=lambda g: (-costs[g], g))
-        load, sob = [0] * S, [0] * len(costs)
-        for g in order:
-            best = max(range(S), key=lambda s: (-load[s], s))  # equal loads -> highest id
-            sob[g] = best
-            load[best] += costs[g]
-        return sob, load
+    def highest_id_on_ties(load):
+        return max(range(len(load)), key=lambda s: (-load[s], s))
 
-    assert lpt_high_tie(c["costs"], c["n_shards"])[0] != c["shard_of_block"]
+    for c in golden["lpt_ties"]:
+        assert oracle.lpt_assign(c["costs"], c["n_shards"])[0] == c["shard_of_block"]
+    monkeypatch.setattr(olpt, "least_loaded", highest_id_on_ties)
+    caught = [oracle.lpt_assign(c["costs"], c["n_shards"])[0] != c["shard_of_block"] for c in golden["lpt_ties"]]
+    assert any(caught)
+    assert caught[0]
 
 
 def test_planted_dropped_scale_is_caught(golden):

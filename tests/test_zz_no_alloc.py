@@ -44,6 +44,8 @@ def test_noalloc_equals_caller_buffer_path_on_two_calls_in_a_row():
         assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
         assert (out.float() - ref_out.float()).abs().max().item() <= TOL_O[w.dtype]
         assert (lse - ref_lse).abs().max().item() <= TOL_L
+        # same plan, same kernels, same arithmetic: the results are identical bit for bit
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
 def test_noalloc_rejects_problems_larger_than_its_array():
@@ -61,3 +63,26 @@ def test_noalloc_rejects_problems_larger_than_its_array():
         K.splitkv_attention_noalloc(q, pool, pool, table, work, n_items, 1, sum(q_len), max(q_len),
                                     w.block_len, w.scale, w.causal, part_rows, out, lse)
     assert e.value.status == -4 and "scratch" in str(e.value)
+
+
+def test_noalloc_rejects_sizes_that_do_not_match_the_descriptor():
+    """part_rows, total_q and max_q_len are checked against the host descriptor before any
+    work, so a wrong row count cannot make the kernels write past the fixed array."""
+    w = CASES[0]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype)
+    out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device="cuda")
+    lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device="cuda")
+    good = dict(n_items=run.n_items, B=run.B, total_q=run.total_q, max_q_len=run.max_q_len,
+                part_rows=run.part_rows)
+    for bad in ({"part_rows": run.part_rows - 1}, {"part_rows": run.part_rows + 1}, {"part_rows": 1 << 60},
+                {"total_q": run.total_q + 1}, {"max_q_len": run.max_q_len + 1}):
+        a = dict(good, **bad)
+        with pytest.raises(K.SplitKVError) as e:
+            K.splitkv_attention_noalloc(inp.q, inp.k_pool, inp.v_pool, inp.block_table, run.work_host,
+                                        a["n_items"], a["B"], a["total_q"], a["max_q_len"], w.block_len, w.scale,
+                                        w.causal, a["part_rows"], out, lse)
+        assert e.value.status == -1, bad
+    torch.cuda.synchronize()
+    assert K.splitkv_device_status() == 0
