@@ -16,9 +16,10 @@
 //              from the paged pool (3-D maps over [tokens, Hkv, d], 128-byte
 //              swizzle, two 64-column halves per tile) into two-stage rings;
 //   warp 9     TMEM allocation and MMA issue (one elected lane);
-//   warp 10    barrier waits for the MMA warp: it waits on the K/V and P
-//              barriers and hands each ready point to warp 9 through a named
-//              barrier, so the issuing thread never pays an mbarrier wait;
+//   warp 10    barrier waits for the MMA warp: it waits on the K/V and S
+//              barriers, zeroes the V tail of a partial tile and hands each
+//              ready point to warp 9 through a named barrier, so the issuing
+//              thread never pays an mbarrier wait;
 //   warp 11    idle (it completes the third warpgroup).
 // TMEM (512 columns): S_A | O_A | S_B | O_B, 128 fp32 columns each.
 // Per KV tile j and query tile X:
@@ -33,9 +34,11 @@
 // more than 2^8, so P stays <= 256 and the common tile needs no O traffic.
 //
 // Keys past the sequence end (pool slots that may hold anything) get score
-// -inf, and their V rows inside the last 16-key MMA step are zeroed in shared
-// memory before the P.V MMAs, so they contribute exactly nothing.  Every wait
-// has a time limit; on expiry the status word gets bit 2 and the CTA unwinds.
+// -inf, and their V rows in a partial tile are zeroed in shared memory before
+// the P.V MMAs, so they contribute exactly nothing.  Every wait has a time
+// limit; on expiry the status word gets bit 2, the warp stops waiting and
+// stops its TMEM work, but keeps taking part in every named-barrier hand-off,
+// so no other warp blocks on it, and the CTA unwinds at the end.
 
 #include <cmath>
 
@@ -88,7 +91,8 @@ struct Barriers {
   uint64_t s_full[2], o_done[2];  // per query tile
   uint64_t drain;
   uint32_t tmem_base;
-  uint32_t abort;  // set by a warp whose wait timed out, before its last arrival
+  int32_t first;    // the unit has a key tile (sync warp -> MMA warp, before the prologue barrier)
+  int32_t next[2];  // next[t & 1]: tile t + 1 exists (sync warp -> MMA warp, before barrier A of tile t)
 };
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (2 + 2 * kStages) + sizeof(Barriers);
@@ -192,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bar->o_done[x], 1);
     }
     ptx::mbar_init(&bar->drain, 1);
-    bar->abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -281,32 +284,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
     };
-    const int nx = has_b ? 2 : 1;
     if (warp == kSyncWarp) {
       // ------------------------------------------------------------ sync warp
-      // Arrives, in order: once Q and K(0) have landed; then per tile t once
-      // V(t) and K(t+1) have.  Before its tile-t arrival it also sees S_A(t)
-      // complete: S_A(t) is issued only after the MMA warp passed barrier A of
-      // tile t-1, so no arrival of this warp can count toward an earlier tile
-      // (the K/V ring alone would let it run a tile ahead).  On a timeout it
-      // flags the abort, arrives once more and stops.
+      // Takes every mbarrier wait off the MMA warp.  Arrives on the prologue
+      // barrier once Q and K(0) have landed (publishing whether the unit has a
+      // key tile), then per tile t on barrier A once S_A(t) has completed and
+      // V(t), K(t+1) have landed, publishing whether tile t+1 exists.  Seeing
+      // S_A(t) complete keeps it from running a tile ahead: S_A(t) is issued
+      // only after the MMA warp passed barrier A of tile t-1.  In a partial
+      // tile it zeroes the V rows of keys past the end (P is 0 there, and the
+      // slots may hold anything, NaN included).  Once a wait has run out it
+      // stops waiting and zeroing but still takes part in every hand-off, with
+      // bar.sync so that it stays in step with the MMA warp.
       bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_full, 0));
       int32_t nv_cur = 0, nv_next = 0;
-      bool has_cur = ok && next_tile(&nv_cur);
-      if (has_cur) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
-      if (!ok && lane == 0) bar->abort = 1;
+      bool has_cur = next_tile(&nv_cur);
+      if (ok && has_cur) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[0], 0));
+      if (lane == 0) bar->first = has_cur ? 1 : 0;
       __syncwarp();
       ptx::bar_arrive(kBarPrologue, kBarPrologueThreads);
       int32_t t = 0;
-      while (ok && has_cur) {
+      while (has_cur) {
         const bool has_next = next_tile(&nv_next);
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[0], t & 1));
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[0], t & 1));
         if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[t % kStages], (t / kStages) & 1));
         if (ok && has_next)
           ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1));
-        if (!ok && lane == 0) bar->abort = 1;
+        if (ok && nv_cur < kN) {
+          uint8_t* vtile = sv + (t % kStages) * kTileBytes;
+          const int cc = lane & 15;  // 16-byte piece of a 256-byte row (two swizzled halves)
+          for (int r = nv_cur + (lane >> 4); r < kN; r += 2)
+            reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128)[cc & 7] = make_uint4(0, 0, 0, 0);
+          tc::fence_proxy_async_smem();  // visible to the tensor cores' reads
+        }
+        if (lane == 0) bar->next[t & 1] = has_next ? 1 : 0;
         __syncwarp();
-        ptx::bar_arrive(kBarTileA, kBarTileAThreads);
+        if (ok)
+          ptx::bar_arrive(kBarTileA, kBarTileAThreads);
+        else
+          ptx::bar_sync(kBarTileA, kBarTileAThreads);
         ++t;
         has_cur = has_next;
         nv_cur = nv_next;
@@ -314,10 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     } else {
     // ------------------------------------------------------------------ MMA
-    // Lane 0 issues every tcgen05.mma and commit; the warp learns that a tile is
-    // ready from a named barrier (far cheaper than an mbarrier wait, and the
-    // tensor pipe drains while the issuing thread waits).  Commits are kept
-    // to two a tile.
+    // Lane 0 issues every tcgen05.mma and commit.  An MMA costs the issuing
+    // thread most of the 64 clk the tensor pipe takes to run it, so the loop
+    // does nothing else per tile: two named-barrier waits (cheap once the
+    // hand-off is there), one shared-memory word, the A and B bursts written
+    // out with their tile index fixed, two commits.  Partial tiles need no
+    // branch here (the sync warp zeroed their tail of V); the roles whose waits
+    // ran out keep taking part in the hand-offs, so no abort test either.
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
     const uint32_t idesc_pv = tc::idesc_bf16_f32(kMT, kD, false, true);
     // Descriptors of every operand tile, built once; an MMA only adds an offset.
@@ -326,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const tc::Desc desc_v0 = tc::split(tc::smem_desc(ptx::smem_addr(sv), kHalfBytes, 1024, tc::kSwizzle128B));
     constexpr uint32_t kTile16 = kTileBytes >> 4;  // one tile, in descriptor address units
     // S_X = Q_X K^T for KV tile t (K in stage t % kStages); lane 0 only
-    auto issue_s = [&](int x, int32_t t) {
+    auto issue_s = [&](const int x, const int32_t t) {
       const uint32_t qoff = x * kTile16, koff = (t % kStages) * kTile16;
       const uint32_t d_col = tmem + col_s(x);
 #pragma unroll
@@ -336,71 +355,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::commit(&bar->s_full[x]);
     };
-    volatile uint32_t* abort_flag = &bar->abort;
-    int32_t nv_cur = 0, nv_next = 0;
-    bool has_cur = next_tile(&nv_cur);
-    ptx::bar_sync(kBarPrologue, kBarPrologueThreads);  // Q, K(0)
-    bool ok = *abort_flag == 0;
-    int32_t t = 0;
-    if (ok && has_cur) {
+    // O_X (+)= P_X V(t), P_X from TMEM, V in stage t % kStages; tile 0 starts the sum
+    auto issue_pv = [&](const int x, const int32_t t) {
+      const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x), voff = (t % kStages) * kTile16;
+#pragma unroll
+      for (int kk = 0; kk < kN / 16; ++kk)
+        tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+    };
+    ptx::bar_sync(kBarPrologue, kBarPrologueThreads);  // Q, K(0); bar->first
+    if (*reinterpret_cast<volatile int32_t*>(&bar->first) != 0) {
       tc::fence_after_sync();
       if (lane == 0) {
-        for (int x = 0; x < nx; ++x) issue_s(x, 0);
+        issue_s(0, 0);
+        if (has_b) issue_s(1, 0);
       }
       __syncwarp();
-    }
-    while (has_cur && ok) {
-      const bool has_next = next_tile(&nv_next);
-      const int vs = t % kStages;
-      ptx::bar_sync(kBarTileA, kBarTileAThreads);  // V(t), K(t+1), P_A(t)
-      if (*abort_flag != 0) { ok = false; break; }
-      uint8_t* vtile = sv + vs * kTileBytes;
-      const int ksteps = (nv_cur + 15) >> 4;
-      if (nv_cur < ksteps * 16) {
-        // zero the V rows of keys past the end inside the last 16-key step
-        for (int r = nv_cur + (lane >> 4); r < ksteps * 16; r += 2) {
-          const int cc = lane & 15;
-          uint4* dst = reinterpret_cast<uint4*>(vtile + (cc < 8 ? 0 : kHalfBytes) + r * 128) + (cc & 7);
-          *dst = make_uint4(0, 0, 0, 0);
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-      }
-      const uint32_t voff = vs * kTile16;
-      for (int x = 0; x < nx; ++x) {
-        // O_X += P_X V_t, then S_X of the next tile (same TMEM columns: the MMAs run in order)
-        if (x == 1) {
-          ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t)
-          if (*abort_flag != 0) { ok = false; break; }
-        }
+      for (int32_t t = 0;; ++t) {
+        ptx::bar_sync(kBarTileA, kBarTileAThreads);  // P_A(t); V(t), K(t+1) landed; bar->next
+        const bool more = *reinterpret_cast<volatile int32_t*>(&bar->next[t & 1]) != 0;
         tc::fence_after_sync();
         if (lane == 0) {
-          const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x);
-          if (ksteps == kN / 16 && t > 0) {
-#pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, 1u);
-          } else {
-            for (int kk = 0; kk < ksteps; ++kk)
-              tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv,
-                              (t > 0 || kk > 0) ? 1u : 0u);
-          }
           // While tiles follow, the next S_X commit also covers this PV_X (a
           // commit tracks every earlier MMA of this thread); only the last PV
           // needs its own signal, for the epilogue.
-          if (has_next)
-            issue_s(x, t + 1);
+          issue_pv(0, t);
+          if (more)
+            issue_s(0, t + 1);
           else
-            tc::commit(&bar->o_done[x]);
+            tc::commit(&bar->o_done[0]);
         }
         __syncwarp();
+        if (has_b) {
+          ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t)
+          tc::fence_after_sync();
+          if (lane == 0) {
+            issue_pv(1, t);
+            if (more)
+              issue_s(1, t + 1);
+            else
+              tc::commit(&bar->o_done[1]);
+          }
+          __syncwarp();
+        }
+        if (!more) break;
       }
-      if (!ok) break;
-      ++t;
-      has_cur = has_next;
-      nv_cur = nv_next;
     }
-    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     // all MMAs issued by this warp have completed before TMEM is released
     if (lane == 0) tc::commit(&bar->drain);
     __syncwarp();
@@ -426,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;
     int32_t t = 0;
     bool ok = true;
-    for (int32_t bi = 0; bi < blk_cnt && ok; ++bi) {
+    for (int32_t bi = 0; bi < blk_cnt; ++bi) {
       int32_t lo, n;
       bool bad;
       const int32_t phys = walk.block(bi, &lo, &n, &bad);
@@ -435,13 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t pos0 = lo + off;
         const int32_t nvalid = min(kN, n - off);
         // waits and TMEM accesses stay warp-uniform (tcgen05.ld/st are warp-collective)
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1))) {
-          // the MMA warp may be waiting for this tile: flag the abort, arrive, stop
-          if (lane == 0) bar->abort = 1;
-          __syncwarp();
-          ptx::bar_arrive(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
-          ok = false;
-          break;
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[x], t & 1));
+        if (!ok) {
+          // a wait ran out: no more TMEM work, but every hand-off still takes
+          // place (bar.sync keeps this warp in step with the MMA warp)
+          ptx::bar_sync(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
+          continue;
         }
         if (release_kv && lane == 0) ptx::mbar_arrive(&bar->kv_free[t % kStages]);  // release t
         tc::fence_after_sync();
