@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (has_cur) {
       ok = wait_all(&bar->k_full[0], 0) && wait_all(&bar->v_full[0], 0);
       tc::fence_after_sync();
-      if (ok && lane == 0) {
+      if (ok && tc::elect_one()) {
         issue_s(0);
         issue_dp(0);
       }
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && has_one) {
         ok = wait_all(&bar->k_full[1 % kKStages], 0);
         tc::fence_after_sync();
-        if (ok && lane == 0) issue_s(1);
+        if (ok && tc::elect_one()) issue_s(1);
         __syncwarp();
       }
     }
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t info = bar->tinfo[t & 1];
       const int32_t nv_cur = static_cast<int32_t>(info & 0xffffu);
       const bool has_next = (info >> 16) & 1u, has_next2 = (info >> 17) & 1u;
-      if (has_next && lane == 0) issue_dp(t + 1);
+      if (has_next && tc::elect_one()) issue_dp(t + 1);
       __syncwarp();
       if (!wait_all(&bar->ds_full, t & 1)) {
         ok = false;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
+      if (tc::elect_one()) {
         for (int kk = 0; kk < ksteps; ++kk)
           tc::mma_ts_fast(tmem + kColDQ, tmem + kColS0 + 128 * (t & 1) + 8 * kk, dk_mn,
                           ks * kTile16 + kk * (2048 >> 4), idesc_dq, (t > 0 || kk > 0) ? 1u : 0u);
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       has_cur = has_next;
     }
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
-    if (lane == 0) tc::commit(&bar->drain);
+    if (tc::elect_one()) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   } else {
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
            __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rt % kQdStages], (rt / kQdStages) & 1));
       if (!ok) break;
       tc::fence_after_sync();
-      if (lane == 0) issue_s(rt % kQdStages, rt & 1);
+      if (tc::elect_one()) issue_s(rt % kQdStages, rt & 1);
       __syncwarp();
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
         const int s = rt % kQdStages, b = rt & 1;
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::fence_after_sync();
-          if (lane == 0) issue_s(rn % kQdStages, rn & 1);
+          if (tc::elect_one()) issue_s(rn % kQdStages, rn & 1);
           __syncwarp();
         }
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full[b], (rt >> 1) & 1))) {
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        if (lane == 0) {
+        if (tc::elect_one()) {
           const uint32_t qoff = s * (kTile64 >> 4);
 #pragma unroll
           for (int kk = 0; kk < kRowsB / 16; ++kk)
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++kt;
     }
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
-    if (lane == 0) tc::commit(&bar->drain);
+    if (tc::elect_one()) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   } else {

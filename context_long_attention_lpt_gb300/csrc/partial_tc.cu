@@ -15,7 +15,7 @@
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
 //              from the paged pool (3-D maps over [tokens, Hkv, d], 128-byte
 //              swizzle, two 64-column halves per tile) into two-stage rings;
-//   warp 9     TMEM allocation and MMA issue (one elected lane);
+//   warp 9     TMEM allocation and MMA issue (one lane, chosen by elect.sync);
 //   warp 10    barrier waits for the MMA warp: it waits on the K/V and S
 //              barriers, zeroes the V tail of a partial tile and hands each
 //              ready point to warp 9 through a named barrier, so the issuing
@@ -330,9 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     } else {
     // ------------------------------------------------------------------ MMA
-    // Lane 0 issues every tcgen05.mma and commit.  An MMA costs the issuing
-    // thread most of the 64 clk the tensor pipe takes to run it, so the loop
-    // does nothing else per tile: two named-barrier waits (cheap once the
+    // One elected lane issues every tcgen05.mma and commit (elect.sync keeps
+    // the operands on the uniform datapath: an MMA then costs the issuing
+    // thread about 17 clk against 48 under a lane test, next to the 64 clk the
+    // tensor pipe takes to run it).  The loop does nothing else per tile: two named-barrier waits (cheap once the
     // hand-off is there), one shared-memory word, the A and B bursts written
     // out with their tile index fixed, two commits.  Partial tiles need no
     // branch here (the sync warp zeroed their tail of V); the roles whose waits
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::bar_sync(kBarPrologue, kBarPrologueThreads);  // Q, K(0); bar->first
     if (*reinterpret_cast<volatile int32_t*>(&bar->first) != 0) {
       tc::fence_after_sync();
-      if (lane == 0) {
+      if (tc::elect_one()) {
         issue_s(0, 0);
         if (has_b) issue_s(1, 0);
       }
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::bar_sync(kBarTileA, kBarTileAThreads);  // P_A(t); V(t), K(t+1) landed; bar->next
         const bool more = *reinterpret_cast<volatile int32_t*>(&bar->next[t & 1]) != 0;
         tc::fence_after_sync();
-        if (lane == 0) {
+        if (tc::elect_one()) {
           // While tiles follow, the next S_X commit also covers this PV_X (a
           // commit tracks every earlier MMA of this thread); only the last PV
           // needs its own signal, for the epilogue.
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_b) {
           ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t)
           tc::fence_after_sync();
-          if (lane == 0) {
+          if (tc::elect_one()) {
             issue_pv(1, t);
             if (more)
               issue_s(1, t + 1);
@@ -400,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!more) break;
       }
     }
-    // all MMAs issued by this warp have completed before TMEM is released
-    if (lane == 0) tc::commit(&bar->drain);
+    // all MMAs issued by this warp have completed before TMEM is released (the
+    // warp is converged at every elect, so the elected lane is always the same)
+    if (tc::elect_one()) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     }
