@@ -56,7 +56,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--fused", action="store_true",
-                    help="splitkv_attn_fused (one launch with the decode kernel) instead of partial + merge")
+                    help="splitkv_attn_fused (one launch with the decode and tensor-core kernels) instead of partial + merge")
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
                     help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
                          "reduction completion model (splitkv_plan_dcp)")

@@ -148,6 +148,22 @@ extern "C" int splitkv_attn_partial(const void* q, const void* k_pool, const voi
   return SPLITKV_OK;
 }
 
+extern "C" int splitkv_fused_launches(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t max_q_len,
+                                      int32_t n_items, int32_t dtype, int32_t kernel) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return fail(SPLITKV_ERR_INVALID, "bad head counts");
+  splitkv::PartialArgs a{};
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.block_len = block_len;
+  a.max_q_len = max_q_len;
+  a.n_items = n_items;
+  a.dtype = dtype;
+  const int k = pick_kernel(a, kernel);
+  splitkv::clear_error();
+  return ((k == SPLITKV_KERNEL_DECODE && splitkv::decode_fuses(a)) || k == SPLITKV_KERNEL_TC) ? 1 : 2;
+}
+
 extern "C" int64_t splitkv_ticket_count(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_q_len < 0)
     return fail(SPLITKV_ERR_INVALID, "splitkv_ticket_count: bad arguments");
@@ -178,7 +194,7 @@ extern "C" int splitkv_attn_fused(const void* q, const void* k_pool, const void*
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int k = pick_kernel(a, kernel);
-  if (k == SPLITKV_KERNEL_DECODE && splitkv::decode_fuses(a)) {
+  if ((k == SPLITKV_KERNEL_DECODE && splitkv::decode_fuses(a)) || k == SPLITKV_KERNEL_TC) {
     a.fused = 1;
     a.tickets = tickets;
     a.out = out;

@@ -44,6 +44,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "merge_row.cuh"
 #include "ptx.cuh"
 #include "status.h"
 #include "tc_ptx.cuh"
@@ -68,6 +69,7 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9, kSyncWarp = 10;
 // P_A(t) written (the four softmax warps of A) and V(t), K(t+1) landed (sync
 // warp);  P_B(t) written (the four softmax warps of B).
 constexpr int kBarPrologue = 1, kBarTileA = 2, kBarTileB = 3;
+constexpr int kBarMerge = 4;  // the softmax warps, around the in-launch merge's ticket
 constexpr int kBarPrologueThreads = 64, kBarTileAThreads = 192, kBarTileBThreads = 160;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
@@ -93,6 +95,7 @@ struct Barriers {
   uint32_t tmem_base;
   int32_t first;    // the unit has a key tile (sync warp -> MMA warp, before the prologue barrier)
   int32_t next[2];  // next[t & 1]: tile t + 1 exists (sync warp -> MMA warp, before barrier A of tile t)
+  int32_t last;     // in-launch merge: this CTA took the last ticket of its unit
 };
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes * (2 + 2 * kStages) + sizeof(Barriers);
@@ -595,6 +598,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (row_valid) a.lse_part[orow] = l > 0.f ? (m_used * c + __log2f(l)) * kLn2 : -INFINITY;
+
+    if (a.fused) {
+      // ---- in-launch merge: the last CTA of each (sequence, K/V head, 256-row
+      // unit) merges the unit's rows over the sequence's items.  The softmax
+      // warps wrote this CTA's partial rows; each publishes them (fence), then
+      // one thread takes a ticket from the unit's counter (the usual
+      // fence-then-count pattern).  No CTA waits for another.
+      const int merge_threads = has_b ? 2 * kMT : kMT;
+      __threadfence();
+      ptx::bar_sync(kBarMerge, merge_threads);
+      // the unit's coordinates again, from the launch index (nothing kept live across the main loop)
+      const int64_t um = blockIdx.x;
+      const int32_t m_utile = static_cast<int32_t>(um % units_per_item);
+      const int32_t m_kvh = static_cast<int32_t>((um / units_per_item) % a.Hkv);
+      const int32_t m_seq = __ldg(wv.item(static_cast<int32_t>(um / (static_cast<int64_t>(units_per_item) * a.Hkv))) + kItSeq);
+      const int32_t m_cu = __ldg(wv.seq(m_seq) + kSqCuQ);
+      const int32_t m_r0 = m_utile * kM;
+      const int32_t m_rows = min(kM, __ldg(wv.seq(m_seq) + kSqQLen) * G - m_r0);
+      const int32_t p0 = __ldg(wv.seq(m_seq) + kSqItemPtr), p1 = __ldg(wv.seq(m_seq + 1) + kSqItemPtr);
+      uint32_t* ticket = a.tickets + (static_cast<int64_t>(m_seq) * a.Hkv + m_kvh) * units_per_item + m_utile;
+      if (threadIdx.x == 0) {
+        const uint32_t taken = atomicAdd(ticket, 1u);
+        const bool last = taken == static_cast<uint32_t>(p1 - p0 - 1);
+        if (last) *ticket = 0u;  // every item's CTA has counted: ready for the next launch
+        __threadfence();
+        bar->last = last ? 1 : 0;
+      }
+      ptx::bar_sync(kBarMerge, merge_threads);
+      if (*reinterpret_cast<volatile int32_t*>(&bar->last) != 0) {
+        // one warp per (token, head) row of the unit, the partials read through L2
+        for (int32_t r = warp; r < m_rows; r += merge_threads / 32) {
+          const int32_t rr = m_r0 + r, tok = rr / G, h = m_kvh * G + rr % G;
+          merge_row<__nv_bfloat16, kD, true>(a.o_part, a.lse_part, wv, p0, p1, tok, h, a.Hq,
+                                             static_cast<int64_t>(m_cu + tok) * a.Hq + h,
+                                             static_cast<__nv_bfloat16*>(a.out), a.lse_out);
+        }
+      }
+    }
   }
   }
 

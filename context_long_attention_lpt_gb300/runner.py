@@ -128,7 +128,9 @@ class SplitKVAttention:
 
     def fuses_in_one_launch(self):
         """Whether splitkv_attn_fused merges inside the partial kernel's launch for this shape."""
-        return self.kernel_used() == _k.KERNEL_DECODE
+        code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
+        return _k.splitkv_fused_launches(self.Hq, self.Hkv, self.d, self.block_len, self.max_q_len, self.n_items,
+                                         code, self.kernel) == 1
 
     # device steps -----------------------------------------------------------
     def _begin(self, stream):

@@ -39,6 +39,7 @@ _SIGNATURES = {
                                              _i32, _p]),
     "splitkv_merge": (ctypes.c_int, [_p, _p, _i64, _p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]),
     "splitkv_ticket_count": (_i64, [_i32, _i32, _i32, _i32]),
+    "splitkv_fused_launches": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "splitkv_attn_fused": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _i32, _f32, _i32, _i32, _p, _p, _i64, _p, _i64, _p, _p, _i32,
                                           _p]),
@@ -221,9 +222,15 @@ def splitkv_ticket_count(B, Hq, Hkv, max_q_len):
     return _check("splitkv_ticket_count", lib().splitkv_ticket_count(B, Hq, Hkv, max_q_len))
 
 
+def splitkv_fused_launches(Hq, Hkv, d, block_len, max_q_len, n_items, dtype, kernel=KERNEL_AUTO):
+    """1 when splitkv_attn_fused merges inside the partial kernel's launch, else 2."""
+    return _check("splitkv_fused_launches",
+                  lib().splitkv_fused_launches(Hq, Hkv, d, block_len, max_q_len, n_items, dtype, kernel))
+
+
 def splitkv_attn_fused(q, k_pool, v_pool, block_table, work, n_items, B, total_q, max_q_len, block_len, scale,
                        causal, o_part, lse_part, tickets, out, lse_out, kernel=KERNEL_AUTO, stream=None):
-    """Partial attention + merge (one launch with the decode kernel); tickets: zeroed int32/uint32 device
+    """Partial attention + merge (one launch with the decode and tensor-core kernels); tickets: zeroed int32/uint32 device
     tensor of at least splitkv_ticket_count(...) elements, left zeroed."""
     for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
                     ("work", work), ("o_part", o_part), ("lse_part", lse_part), ("tickets", tickets),

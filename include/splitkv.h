@@ -165,14 +165,25 @@ int splitkv_attn_partial(const void* q, const void* k_pool, const void* v_pool,
 /* Counters splitkv_attn_fused needs: B * Hkv * max(1, ceil(max_q_len*(Hq/Hkv)/256)). */
 int64_t splitkv_ticket_count(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_q_len);
 
+/* Launches splitkv_attn_fused makes for a shape and kernel choice: 1 when the
+ * chosen kernel merges inside its own launch (decode kernel with at most 2048
+ * items, tensor-core kernel), 2 otherwise (partial, then merge).  Negative
+ * status for bad head counts. */
+int splitkv_fused_launches(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t max_q_len,
+                           int32_t n_items, int32_t dtype, int32_t kernel);
+
 /* Steps 3 and 4 in one call (Split-KV card, "All Facts": exact, "Timeline":
  * query-sized partials): the partial attention of splitkv_attn_partial and the
  * merge of splitkv_merge, with the same arguments and results.  With the decode
- * kernel both happen in ONE launch: each CTA writes its partial rows, publishes
- * them (memory fence) and takes a ticket from the counter of its (sequence, K/V
- * head) group with an atomic add; the CTA that takes the last ticket merges the
- * group's partials into out / lse_out and sets the counter back to zero.  No CTA
- * waits for another.  Other kernels run the partial and merge launches in turn.
+ * and tensor-core kernels both happen in ONE launch: each CTA writes its
+ * partial rows, publishes them (memory fence) and takes a ticket from the
+ * counter of its group with an atomic add - a (sequence, K/V head) for the
+ * decode kernel, a (sequence, K/V head, 256-row unit) for the tensor-core
+ * kernel; the CTA that takes the last ticket sets the counter back to zero and
+ * merges the group's partials into out / lse_out.  No CTA waits for another.
+ * The tensor-core kernel's merge computes each row exactly as splitkv_merge
+ * does, so the two paths give the same bits.  The generic CUDA-core kernel runs
+ * the partial and merge launches in turn (splitkv_fused_launches tells which).
  *   tickets (device, caller-owned): n_tickets >= splitkv_ticket_count(...)
  *   uint32 counters, all zero before the first call; every completed call leaves
  *   them zero again.  After a call that reported a device error (status word),

@@ -155,10 +155,12 @@ def test_bad_arguments_raise_before_launch():
         run_cuda(w2, kernel=K.KERNEL_TC)
 
 
-@pytest.mark.parametrize("name", ["decode_small", "decode_gqa8", "shortq_small", "tiny"])
+@pytest.mark.parametrize("name", ["decode_small", "decode_gqa8", "shortq_small", "varlen_small", "largest_small",
+                                  "causal_empty_units", "tiny"])
 def test_fused_single_launch_matches_oracle(name):
-    """splitkv_attn_fused: the decode kernel merges in its own launch (last CTA per group);
-    other kernels fall back to two launches.  Two calls in a row: the tickets return to zero."""
+    """splitkv_attn_fused: the decode and tensor-core kernels merge in their own launch (the
+    last CTA per group); the CUDA-core kernel falls back to two launches.  Two calls in a row:
+    the tickets return to zero."""
     w = SMALL[name]
     inp = wl.make_inputs(w, device="cuda", poison_tail=True)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
@@ -235,3 +237,40 @@ def test_runner_on_a_side_stream():
     side.synchronize()
     assert torch.isfinite(dq).all()
     assert K.splitkv_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("name", ["shortq_small", "varlen_small", "largest_small", "causal_empty_units"])
+def test_fused_tensor_core_equals_two_launches_bit_for_bit(name):
+    """The tensor-core kernel's in-launch merge computes every row as the merge kernel does."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    two = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype)
+    one = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=True)
+    assert one.kernel_used() == K.KERNEL_TC and one.fuses_in_one_launch()
+    o2, l2 = two(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    o1, l1 = one(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert int(one.tickets.abs().sum()) == 0
+    assert K.splitkv_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["largest", "varlen"])
+def test_fused_tensor_core_full_size(name):
+    """Full-size tensor-core workloads through the one-launch path: sampled rows against the
+    oracle, tickets back to zero after two calls."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=True)
+    assert run.fuses_in_one_launch()
+    for _ in range(2):
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    eo, el = compare_rows(inp, out, lse, sample_rows(inp, 48, seed=9))
+    assert_close(w, eo, el, f"fused {name}")
+    assert int(run.tickets.abs().sum()) == 0
+    assert K.splitkv_device_status() == 0

@@ -244,3 +244,15 @@ def test_dcp_extremes(k):
     assert t == best and max(load) == best
     s1, sob1, _, _ = k.splitkv_plan_dcp(q, kv, w.block_len, w.causal, w.n_shards, 1.0, 1e12)
     assert s1 == 1 and set(sob1.tolist()) == {0}
+
+
+def test_fused_launch_count_by_kernel(k):
+    """splitkv_attn_fused merges inside the launch for the decode and tensor-core kernels."""
+    BF, F32 = k.SPLITKV_BF16, k.SPLITKV_F32
+    assert k.splitkv_fused_launches(32, 8, 128, 256, 1, 128, BF) == 1          # decode kernel
+    assert k.splitkv_fused_launches(32, 8, 128, 256, 1, 5000, BF) == 2         # decode, too many items
+    assert k.splitkv_fused_launches(32, 8, 128, 1024, 512, 64, BF) == 1        # tensor cores
+    assert k.splitkv_fused_launches(4, 4, 64, 128, 16, 4, F32) == 2            # CUDA-core kernel
+    assert k.splitkv_fused_launches(32, 8, 128, 1024, 512, 64, BF, k.KERNEL_SIMT) == 2
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_fused_launches(30, 8, 128, 1024, 512, 64, BF)
