@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
                     help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
                          "reduction completion model (splitkv_plan_dcp)")
+    ap.add_argument("--item-blocks", type=int, default=0,
+                    help="cut work items into runs of at most this many blocks (0: one item per shard and "
+                         "sequence)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (delta, per-shard dK/dV + partial dQ, dQ reduce) instead")
     ap.add_argument("--context", type=int, default=None,
@@ -279,7 +282,8 @@ def measure_forward(args, dctx, name, dev, headline=False):
     alpha, beta, gamma = dcp_model(w)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
                            inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
-                           planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma)
+                           planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma,
+                           item_blocks=args.item_blocks if headline else 0)
     fused_one_launch = run.fused and run.fuses_in_one_launch()
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")

@@ -213,17 +213,21 @@ extern "C" int64_t splitkv_work_words(int64_t n_blocks, int32_t B) {
          (splitkv::kItemWords + 2) * n_blocks;
 }
 
-extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B,
-                                  int32_t block_len, const int64_t* block_cost,
-                                  const int32_t* shard_of_block, int64_t n_blocks,
-                                  int32_t n_shards, int32_t* work, int64_t work_words,
-                                  int32_t* n_items_out, int64_t* part_rows_out) {
+namespace {
+
+// Work lists of a plan; max_item_blocks > 0 cuts every (shard, sequence) run of
+// blocks into items of at most that many blocks (0: one item per pair).
+int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
+               const int64_t* block_cost, const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+               int32_t max_item_blocks, int32_t* work, int64_t work_words, int32_t* n_items_out,
+               int64_t* part_rows_out) {
   using namespace splitkv;
   int st = 0;
   if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
   if (!work || !n_items_out || !part_rows_out || (n_blocks > 0 && (!block_cost || !shard_of_block)))
     return fail(SPLITKV_ERR_INVALID, "splitkv_build_work: null argument");
   if (n_shards <= 0) return fail(SPLITKV_ERR_INVALID, "n_shards must be positive");
+  if (max_item_blocks < 0) return fail(SPLITKV_ERR_INVALID, "max_item_blocks must be >= 0");
   const int64_t need = splitkv_work_words(n_blocks, B);
   if (need < 0) return static_cast<int>(need);
   if (work_words < need)
@@ -267,7 +271,8 @@ extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, i
   for (int64_t i = 0; i < n_blocks;) {
     int64_t j = i;
     Item it{shard_of_block[idx[i]], seq_of[idx[i]], i, 0, 0};
-    while (j < n_blocks && shard_of_block[idx[j]] == it.shard && seq_of[idx[j]] == it.seq) {
+    while (j < n_blocks && shard_of_block[idx[j]] == it.shard && seq_of[idx[j]] == it.seq &&
+           (max_item_blocks == 0 || j - i < max_item_blocks)) {
       it.cost += block_cost[idx[j]];
       ++j;
     }
@@ -350,6 +355,26 @@ extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, i
   *part_rows_out = part_row;
   splitkv::clear_error();
   return SPLITKV_OK;
+}
+
+}  // namespace
+
+extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                                  int32_t block_len, const int64_t* block_cost,
+                                  const int32_t* shard_of_block, int64_t n_blocks,
+                                  int32_t n_shards, int32_t* work, int64_t work_words,
+                                  int32_t* n_items_out, int64_t* part_rows_out) {
+  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, 0, work,
+                    work_words, n_items_out, part_rows_out);
+}
+
+extern "C" int splitkv_build_work_split(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                                        int32_t block_len, const int64_t* block_cost,
+                                        const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+                                        int32_t max_item_blocks, int32_t* work, int64_t work_words,
+                                        int32_t* n_items_out, int64_t* part_rows_out) {
+  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, max_item_blocks,
+                    work, work_words, n_items_out, part_rows_out);
 }
 
 extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,

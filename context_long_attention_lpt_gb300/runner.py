@@ -27,7 +27,7 @@ from . import splitkv as _k
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
                  device="cuda", kernel=_k.KERNEL_AUTO, fused=False, planner="lpt", dcp_alpha=1.0,
-                 dcp_beta=0.0, dcp_gamma=0.0):
+                 dcp_beta=0.0, dcp_gamma=0.0, item_blocks=0):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -44,6 +44,7 @@ class SplitKVAttention:
         self.planner = planner
         self.dcp_alpha, self.dcp_beta, self.dcp_gamma = float(dcp_alpha), float(dcp_beta), float(dcp_gamma)
         self.n_shards_used = self.n_shards
+        self.item_blocks = int(item_blocks)  # > 0: work items of at most this many blocks
         self._tickets = None
         self._grad_pools = None
         self.total_q = sum(self.q_len)
@@ -73,9 +74,14 @@ class SplitKVAttention:
             self.n_shards_used, self.shard_of_block, self.shard_load, self.modeled_time = _k.splitkv_plan_dcp(
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
                 self.dcp_beta, self.dcp_gamma)
-        work, self.n_items, self.part_rows = _k.splitkv_build_work(
-            self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
-            self.n_shards)
+        if self.item_blocks > 0:
+            work, self.n_items, self.part_rows = _k.splitkv_build_work_split(
+                self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
+                self.n_shards, self.item_blocks)
+        else:
+            work, self.n_items, self.part_rows = _k.splitkv_build_work(
+                self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
+                self.n_shards)
         slot = self._ring[self._ring_next]
         self._ring_next = (self._ring_next + 1) % len(self._ring)
         if slot[1] is not None:

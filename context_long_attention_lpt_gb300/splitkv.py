@@ -32,6 +32,7 @@ _SIGNATURES = {
                                         ctypes.c_double, _p, _i64, _p, _p, _p]),
     "splitkv_work_words": (_i64, [_i64, _i32]),
     "splitkv_build_work": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _p, _i64, _p, _p]),
+    "splitkv_build_work_split": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _p, _i64, _p, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "splitkv_backward_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32]),
     "splitkv_attn_partial": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32,
@@ -168,6 +169,21 @@ def splitkv_build_work(q_len, kv_len, block_len, block_cost, shard_of_block, n_s
            lib().splitkv_build_work(_ptr(q), _ptr(kv), len(q), block_len, _ptr(c), _ptr(sob), len(c),
                                     n_shards, _ptr(work), words, ctypes.byref(n_items),
                                     ctypes.byref(part_rows)))
+    return work, n_items.value, part_rows.value
+
+
+def splitkv_build_work_split(q_len, kv_len, block_len, block_cost, shard_of_block, n_shards, max_item_blocks):
+    """Returns (work int32 array, n_items, part_rows); items of at most max_item_blocks blocks."""
+    q, kv = _np(q_len, np.int32), _np(kv_len, np.int32)
+    c, sob = _np(block_cost, np.int64), _np(shard_of_block, np.int32)
+    words = splitkv_work_words(len(c), len(q))
+    work = np.zeros(words, dtype=np.int32)
+    n_items = ctypes.c_int32(0)
+    part_rows = ctypes.c_int64(0)
+    _check("splitkv_build_work_split",
+           lib().splitkv_build_work_split(_ptr(q), _ptr(kv), len(q), block_len, _ptr(c), _ptr(sob), len(c),
+                                          n_shards, int(max_item_blocks), _ptr(work), words,
+                                          ctypes.byref(n_items), ctypes.byref(part_rows)))
     return work, n_items.value, part_rows.value
 
 

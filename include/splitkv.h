@@ -134,6 +134,21 @@ int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B,
                        int32_t* work, int64_t work_words, int32_t* n_items,
                        int64_t* part_rows);
 
+/* splitkv_build_work with every (shard, sequence) run of blocks cut into items
+ * of at most max_item_blocks blocks (in the run's ascending block order; 0: no
+ * cut, the same descriptor as splitkv_build_work).  The plan is unchanged:
+ * each item still belongs to one shard, and the merge reduces the extra
+ * partial rows exactly like those of other shards (Split-KV card, "All
+ * Facts": any split of a sequence's keys merges to the unsharded result).
+ * More, shorter items give the device more, shorter units of work: the last
+ * partly filled wave of CTAs gets shorter.  Same buffers and statuses as
+ * splitkv_build_work; splitkv_work_words bounds the size for any cut. */
+int splitkv_build_work_split(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                             int32_t block_len, const int64_t* block_cost,
+                             const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+                             int32_t max_item_blocks, int32_t* work, int64_t work_words,
+                             int32_t* n_items, int64_t* part_rows);
+
 /* Which kernel SPLITKV_KERNEL_AUTO picks for a shape (a SPLITKV_KERNEL_* value). */
 int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len,
                         int32_t max_q_len, int32_t dtype);

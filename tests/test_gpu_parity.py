@@ -274,3 +274,40 @@ def test_fused_tensor_core_full_size(name):
     assert_close(w, eo, el, f"fused {name}")
     assert int(run.tickets.abs().sum()) == 0
     assert K.splitkv_device_status() == 0
+
+
+@pytest.mark.parametrize("name,max_blocks", [("decode_small", 2), ("decode_gqa8", 1), ("shortq_small", 1),
+                                             ("varlen_small", 2)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_split_items_merge_to_the_unsharded_result(name, max_blocks, fused):
+    """Work items cut into runs of a few blocks (more partial rows per sequence) give the
+    oracle's unsharded attention, two launches and one."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=fused, item_blocks=max_blocks)
+    whole = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                             inp.q.dtype)
+    assert run.n_items > whole.n_items
+    o_ref, l_ref = full_reference(inp)
+    for _ in range(2):
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        torch.cuda.synchronize()
+        eo, el = max_errors(out, lse, o_ref, l_ref)
+        assert_close(w, eo, el, f"{name} items of {max_blocks} blocks, fused={fused}")
+    if fused and run.fuses_in_one_launch():
+        assert int(run.tickets.abs().sum()) == 0
+    assert K.splitkv_device_status() == 0
+
+
+def test_split_items_decode_full_size():
+    w = wl.WORKLOADS["decode"]
+    inp = wl.make_inputs(w, device="cuda")
+    for fused in (False, True):
+        run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                               inp.q.dtype, fused=fused, item_blocks=2)
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        torch.cuda.synchronize()
+        eo, el = compare_rows(inp, out, lse, sample_rows(inp, 64, seed=5))
+        assert_close(w, eo, el, f"decode, items of 2 blocks, fused={fused}")
+    assert K.splitkv_device_status() == 0

@@ -136,6 +136,50 @@ def test_work_lists_cover_the_plan(k, name):
         assert d["seqs"][b, 0] == sum(q[:b]) and d["seqs"][b, 1] == q[b] and d["seqs"][b, 2] == kv[b]
 
 
+@pytest.mark.parametrize("name,max_blocks", [("decode", 2), ("decode", 3), ("varlen", 5), ("shortq", 1),
+                                             ("largest", 4), ("tiny", 64)])
+def test_split_work_lists_cover_the_plan(k, name, max_blocks):
+    """Items cut to at most max_blocks blocks: per (shard, sequence) their blocks, in order, are the
+    plan's key set of that shard; partial rows stay contiguous; the per-sequence lists hold every item."""
+    w = wl.WORKLOADS[name]
+    q, kv = wl.lengths(w)
+    costs = k.splitkv_block_costs(q, kv, w.block_len, w.causal)
+    sob, _ = k.splitkv_plan(costs, w.n_shards)
+    work, n_items, part_rows = k.splitkv_build_work_split(q, kv, w.block_len, costs, sob, w.n_shards, max_blocks)
+    d = _decode_work(work)
+    assert d["n_items"] == n_items
+    sets = oracle.shard_key_sets(sob.tolist(), kv, w.block_len, w.n_shards)
+    got = {}
+    rows = 0
+    gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
+    item_costs = []
+    for it in d["items"]:
+        shard, seq, off, cnt, prow, clo, chi, _ = it.tolist()
+        assert 0 < cnt <= max_blocks
+        blks = d["blocks"][off: off + cnt].tolist()
+        got.setdefault((shard, seq), []).append(blks)
+        assert prow == rows
+        rows += q[seq]
+        cost = (clo & 0xFFFFFFFF) | (chi << 32)
+        assert cost == sum(costs[gbase[seq] + j] for j in blks)
+        item_costs.append(cost)
+    assert rows == part_rows
+    assert item_costs == sorted(item_costs, reverse=True)
+    for (shard, seq), runs in got.items():
+        # the runs of one (shard, sequence) pair cut its ascending block list in order
+        assert sorted(sum(runs, [])) == sets[shard][seq]
+        assert all(len(r) == max_blocks for r in sorted(runs, key=lambda r: r[0])[:-1])
+    assert sum(len(v) for s in sets for v in s) == sum(len(r) for runs in got.values() for r in runs)
+    for b in range(len(q)):
+        p0, p1 = d["seqs"][b, 3], d["seqs"][b + 1, 3]
+        its = d["seq_items"][p0:p1].tolist()
+        assert sorted(its) == sorted(i for i in range(n_items) if d["items"][i, 1] == b)
+    # no cut reproduces the plain work lists
+    plain = k.splitkv_build_work(q, kv, w.block_len, costs, sob, w.n_shards)
+    same = k.splitkv_build_work_split(q, kv, w.block_len, costs, sob, w.n_shards, 0)
+    assert np.array_equal(plain[0], same[0]) and plain[1:] == same[1:]
+
+
 def test_imbalance_on_workloads(k):
     """The library's max/mean - 1 of the LPT loads equals the oracle's bit for bit; the
     hand-derived values for the workloads are pinned in test_oracle."""
