@@ -43,8 +43,14 @@ constexpr uint32_t kHalfBytes = 128 * 64 * 2;    // 128 rows x 64 bf16: one swiz
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 192;  // warps 0-3: elementwise (one TMEM lane each); 4: TMA; 5: MMA
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+// dQ kernel: warps 0-7 elementwise, two per TMEM lane quarter (warp w: rows of
+// quarter w % 4, key columns w / 4 * 64 .. + 63 of each key tile); 8: TMA; 9: MMA
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kRowWarps = 8;
+// dS (bf16 pairs) of keys 16 kk .. 16 kk + 15, relative to the S columns of the
+// tile: keys 0-63 over columns 0-31, keys 64-127 over columns 64-95 (each row
+// warp writes over the columns it has read; the other half stays intact).
+__device__ __forceinline__ uint32_t ds_col(int kk) { return 8u * kk + (kk >= 4 ? 32u : 0u); }
 
 // TMEM columns of the dK/dV kernel's two fp32 accumulators.
 constexpr uint32_t kColAcc0 = 256, kColAcc1 = 384;
@@ -193,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->s_full[b], 1);
     ptx::mbar_init(&bar->dp_full, 1);
-    ptx::mbar_init(&bar->dp_free, 4);
-    ptx::mbar_init(&bar->ds_full, 4);
+    ptx::mbar_init(&bar->dp_free, kRowWarps);
+    ptx::mbar_init(&bar->ds_full, kRowWarps);
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (tc::elect_one()) {
         for (int kk = 0; kk < ksteps; ++kk)
-          tc::mma_ts_fast(tmem + kColDQ, tmem + kColS0 + 128 * (t & 1) + 8 * kk, dk_mn,
+          tc::mma_ts_fast(tmem + kColDQ, tmem + kColS0 + 128 * (t & 1) + ds_col(kk), dk_mn,
                           ks * kTile16 + kk * (2048 >> 4), idesc_dq, (t > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar->k_free[ks]);
         if (!has_next) tc::commit(&bar->o_done);
@@ -353,8 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   } else {
     // ----------------------------------------------------- row threads (dS)
-    const int32_t row = warp * 32 + lane;  // TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int rq = warp & 3, hh = warp >> 2;  // TMEM lane quarter; 64-key half of each key tile
+    const int32_t row = rq * 32 + lane;       // TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(rq * 32) << 16);
     const bool row_valid = row < n_rows;
     const int32_t token = (r0 + row) / G, h = kvh * G + (r0 + row) % G;
     const int64_t grow = static_cast<int64_t>(cu_q + token) * a.Hq + h;
@@ -377,17 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const int32_t lim = live ? min(nvalid, my_vis - pos0) : 0;  // keys [0, lim) of the tile are seen
-      const uint32_t s_col = kColS0 + 128 * (t & 1);
+      // keys [0, lim) of this warp's 64 columns are seen
+      const int32_t lim = (live ? min(nvalid, my_vis - pos0) : 0) - 64 * hh;
+      const uint32_t s_col = kColS0 + 128 * (t & 1) + 64 * hh, dp_col = kColDPq + 64 * hh;
+      // this warp's 64 columns, 32 at a time; dS (bf16) over the first 32 S
+      // columns of its half, all already read when written
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[2][32], dp[2][32], pk[32];
-        tc::tmem_ld32(lane_addr + s_col + 64 * hh, sr[0]);
-        tc::tmem_ld32(lane_addr + s_col + 64 * hh + 32, sr[1]);
-        tc::tmem_ld32(lane_addr + kColDPq + 64 * hh, dp[0]);
-        tc::tmem_ld32(lane_addr + kColDPq + 64 * hh + 32, dp[1]);
+      for (int q = 0; q < 2; ++q) {
+        uint32_t sr[32], dp[32], pk[16];
+        tc::tmem_ld32(lane_addr + s_col + 32 * q, sr);
+        tc::tmem_ld32(lane_addr + dp_col + 32 * q, dp);
         tc::tmem_ld_wait();
-        if (hh == 1) {  // all of dP(t) is in registers: the next dP may be issued
+        if (q == 1) {  // all of this warp's dP(t) is in registers: the next dP may be issued
           if (warp == 0) {
             if (lane == 0)
               bar->tinfo[t & 1] = static_cast<uint32_t>(nvalid) | (has_next ? 1u << 16 : 0u) |
@@ -401,20 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ptx::mbar_arrive(&bar->dp_free);
         }
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int i = 0; i < 32; i += 2) {
+          const int j = 32 * q + i;
+          float ds[2];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int j = 64 * hh + 32 * q + i;
-            float ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float p = fast_exp2(__uint_as_float(sr[q][i + e]) * c - lc);
-              ds[e] = j + e < lim ? p * (__uint_as_float(dp[q][i + e]) - Dr) : 0.f;
-            }
-            pk[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+          for (int e = 0; e < 2; ++e) {
+            const float p = fast_exp2(__uint_as_float(sr[i + e]) * c - lc);
+            ds[e] = j + e < lim ? p * (__uint_as_float(dp[i + e]) - Dr) : 0.f;
           }
-        // dS as bf16 over S columns [32 hh, 32 hh + 32) of this tile's buffer: all already read
-        tc::tmem_st32(lane_addr + s_col + 32 * hh, pk);
+          pk[i / 2] = pack_bf16(ds[0], ds[1]);
+        }
+        tc::tmem_st16(lane_addr + s_col + 16 * q, pk);
       }
       if (warp == 1 && has_next2 &&
           !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->k_full[(t + 2) % kKStages], ((t + 2) / kKStages) & 1)))
@@ -436,17 +441,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The Q tile is free once o_done is seen (every S MMA has completed): each
       // warp passes 32 rows x 32 columns at a time through its 4 KB of it (16-byte
       // slot y of row k at y ^ (k & 7)) and stores whole 128-byte row pieces.
-      float4* wst = reinterpret_cast<float4*>(sq + warp * 4096);
+      float4* wst = reinterpret_cast<float4*>(sq + (hh * 4 + rq) * 4096);
       int64_t orow_k[8];
       bool valid_k[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int32_t rk = warp * 32 + 4 * i + (lane >> 3);
+        const int32_t rk = rq * 32 + 4 * i + (lane >> 3);
         valid_k[i] = rk < n_rows;
         orow_k[i] = static_cast<int64_t>(part_row + (r0 + rk) / G) * a.Hq + kvh * G + (r0 + rk) % G;
       }
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
         uint32_t acc[32];
         tc::tmem_ld32(lane_addr + kColDQ + 32 * q4, acc);
         tc::tmem_ld_wait();
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {  // no key tile (the Q copy was never waited for) or the waits ran out: direct stores
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
         uint32_t acc[32];
         if (t > 0) {
           tc::tmem_ld32(lane_addr + kColDQ + 32 * q4, acc);
@@ -498,6 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ========================================================== dK / dV kernel
 
 constexpr int kKeySplit = 16;   // CTAs per (item, K/V head); each takes every 16th key tile
+// Warps 0-7: key threads, two per TMEM lane quarter (warp w: keys of quarter w % 4,
+// rows w / 4 * 32 .. + 31 of each 64-row tile); 8: TMA; 9: MMA.
+constexpr int kKvThreads = 320;
+constexpr int kKvProducerWarp = 8, kKvMmaWarp = 9, kKeyWarps = 8;
+// P^T / dS^T (bf16 pairs) of rows 16 kk .. 16 kk + 15, relative to the S^T / dP^T
+// columns of the tile: rows 0-31 over columns 0-15, rows 32-63 over columns 32-47
+// (each key warp writes over the columns it has read; the other half stays intact).
+__device__ __forceinline__ uint32_t pt_col(int kk) { return 8u * kk + (kk >= 2 ? 16u : 0u); }
 constexpr int kRowsB = 64;      // query rows per tile here: two tiles' S^T / dP^T fit in TMEM
 constexpr int kQdStages = 4;    // Q / dO ring: the tile in the elementwise pass, the next one's
                                 // S^T / dP^T in the pipe, and two loading
@@ -523,7 +536,7 @@ struct KvBarriers {
 constexpr uint32_t kStageBytes = 4 * 32 * 32 * 4;
 constexpr size_t kKvSmem = 1024 + 2 * kTileBytes + 2 * kQdStages * kTile64 + kStageBytes + sizeof(KvBarriers);
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
                        float* __restrict__ dk_pool, float* __restrict__ dv_pool,
                        const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
@@ -572,13 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&bar->s_full[b], 1);
-      ptx::mbar_init(&bar->ds_full[b], 4);
+      ptx::mbar_init(&bar->ds_full[b], kKeyWarps);
     }
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kKvMmaWarp) {
     tc::tmem_alloc(&bar->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -587,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_base;
 
-  if (warp == kProducerWarp) {
+  if (warp == kKvProducerWarp) {
     // ------------------------------------------------------------- producer
     // Per key tile: K and V (after the previous key tile's MMAs are done),
     // then every row tile's Q, dO by TMA and L, D by the warp's lanes.
@@ -651,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t v = max(0, rt - kQdStages); v < rt; ++v)
         if (!ptx::mbar_wait(&bar->qd_full[v % kQdStages], (v / kQdStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kKvMmaWarp) {
     // ------------------------------------------------------------------ MMA
     // Row tile r uses the TMEM pair of parity b = r & 1.  S^T(r+1), dP^T(r+1)
     // are issued before waiting for the key threads' pass over tile r, so the
@@ -707,11 +720,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qoff = s * (kTile64 >> 4);
 #pragma unroll
           for (int kk = 0; kk < kRowsB / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColST + 64 * b + 8 * kk, ddo_mn, qoff + kk * (2048 >> 4),
+            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColST + 64 * b + pt_col(kk), ddo_mn, qoff + kk * (2048 >> 4),
                             idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kRowsB / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDPT + 64 * b + 8 * kk, dq_mn, qoff + kk * (2048 >> 4),
+            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDPT + 64 * b + pt_col(kk), dq_mn, qoff + kk * (2048 >> 4),
                             idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&bar->qd_free[s]);
           if (r == n_rt - 1) tc::commit(&bar->o_done);
@@ -726,8 +739,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   } else {
     // ------------------------------------------------ key threads (P^T, dS^T)
-    const int32_t k = warp * 32 + lane;  // TMEM lane = key of the tile
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int kq = warp & 3, hh = warp >> 2;  // TMEM lane quarter; 32-row half of each row tile
+    const int32_t k = kq * 32 + lane;         // TMEM lane = key of the tile
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(kq * 32) << 16);
     const float c = a.scale * kLog2e;
     TileSeq walk = tiles;
     int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
@@ -747,41 +761,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows j of the tile this key contributes to: [jmin, jmax)
         const int32_t jmin = key_valid ? max(0, t_first * G - r * kRowsB) : kRowsB;
         const int32_t jmax = min(kRowsB, rows - r * kRowsB);
-        const float* Ls = bar->ld[s][0];
-        const float* Ds = bar->ld[s][1];
-        uint32_t sr[2][32], dp[2][32], pk[32], dk2[32];
-        tc::tmem_ld32(lane_addr + kColST + 64 * b, sr[0]);
-        tc::tmem_ld32(lane_addr + kColST + 64 * b + 32, sr[1]);
-        tc::tmem_ld32(lane_addr + kColDPT + 64 * b, dp[0]);
-        tc::tmem_ld32(lane_addr + kColDPT + 64 * b + 32, dp[1]);
+        const float* Ls = bar->ld[s][0] + 32 * hh;
+        const float* Ds = bar->ld[s][1] + 32 * hh;
+        const uint32_t st_col = kColST + 64 * b + 32 * hh, dpt_col = kColDPT + 64 * b + 32 * hh;
+        uint32_t sr[32], dp[32], pk[16], dk2[16];
+        tc::tmem_ld32(lane_addr + st_col, sr);
+        tc::tmem_ld32(lane_addr + dpt_col, dp);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int i = 0; i < 32; i += 2) {
+          float p[2], ds[2];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float p[2], ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int j = 32 * q + i + e;
-              const float Lj = Ls[j];
-              const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
-              const float pj = fast_exp2(__uint_as_float(sr[q][i + e]) * c - Lj * kLog2e);
-              p[e] = on ? pj : 0.f;
-              ds[e] = on ? pj * (__uint_as_float(dp[q][i + e]) - Ds[j]) : 0.f;
-            }
-            pk[16 * q + i / 2] = pack_bf16(p[0], p[1]);
-            dk2[16 * q + i / 2] = pack_bf16(ds[0], ds[1]);
+          for (int e = 0; e < 2; ++e) {
+            const int j = 32 * hh + i + e;
+            const float Lj = Ls[i + e];
+            const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
+            const float pj = fast_exp2(__uint_as_float(sr[i + e]) * c - Lj * kLog2e);
+            p[e] = on ? pj : 0.f;
+            ds[e] = on ? pj * (__uint_as_float(dp[i + e]) - Ds[i + e]) : 0.f;
           }
-        // P^T over the S^T columns, dS^T over the dP^T columns (first 32 of 64: all already read)
-        tc::tmem_st32(lane_addr + kColST + 64 * b, pk);
-        tc::tmem_st32(lane_addr + kColDPT + 64 * b, dk2);
+          pk[i / 2] = pack_bf16(p[0], p[1]);
+          dk2[i / 2] = pack_bf16(ds[0], ds[1]);
+        }
+        // P^T over this half's first 16 S^T columns, dS^T over its first 16 dP^T
+        // columns: both already read, and the other half's columns stay intact
+        tc::tmem_st16(lane_addr + st_col, pk);
+        tc::tmem_st16(lane_addr + dpt_col, dk2);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bar->ds_full[b]);
       }
       if (!ok) break;
-      // epilogue: this key's dV and dK = scale * sum dS^T Q
+      // epilogue: this key's dV and dK = scale * sum dS^T Q, by the warps of the
+      // first half (one per lane quarter); the others go on to the next key tile
+      if (hh == 1) {
+        ++kt;
+        continue;
+      }
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, kt & 1))) {
         ok = false;
         break;
@@ -790,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Each chunk of 32 columns goes through this warp's 32 x 32 staging block
       // (16-byte slot x of row k at x ^ (k & 7): no bank conflicts either way), then
       // out as whole 128-byte row pieces, four keys per store instruction.
-      float4* wst = reinterpret_cast<float4*>(stage + warp * 32 * 32);
+      float4* wst = reinterpret_cast<float4*>(stage + kq * 32 * 32);
 #pragma unroll 1
       for (int q4 = 0; q4 < 8; ++q4) {
         const bool is_k = q4 >= 4;
@@ -808,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int kr = 4 * i + (lane >> 3), x = lane & 7;  // key of the warp, 16-byte slot
-          const int key = warp * 32 + kr;
+          const int key = kq * 32 + kr;
           if (key < nv) {
             const int64_t krow = (static_cast<int64_t>(tok) + key) * a.Hkv + kvh;  // pool token tok + key
             reinterpret_cast<float4*>(pool + krow * kD + 32 * (q4 & 3))[x] = wst[kr * 8 + (x ^ (kr & 7))];
@@ -823,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kKvMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -878,7 +895,7 @@ int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, cons
   if (grid_kv > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many backward units");
   e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKvSmem));
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward smem attribute: %s", cudaGetErrorString(e));
-  bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kThreads, kKvSmem, stream>>>(a, lse, delta, dk_pool, dv_pool,
+  bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kKvThreads, kKvSmem, stream>>>(a, lse, delta, dk_pool, dv_pool,
                                                                                      tq64, tdo64, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dK/dV launch: %s", cudaGetErrorString(e));
