@@ -113,30 +113,38 @@ def aggregate(dist_ctx, local_seconds, local_units, device=None):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """nvidia-smi clock / throttle samples (every 20 ms, time-stamped); only the samples taken
+    inside the timed region (mark_start .. mark_end, host clock) are summarised."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id, path):
         self.gpu_id, self.path, self.proc = gpu_id, path, None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
             self.proc = None
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.15)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -145,26 +153,39 @@ class ClockSampler:
         self.f.close()
         return self.summary()
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, smax, reasons, power = [], [], set(), []
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                rows.append((self._stamp(parts[0]), float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1 + 0.02]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: the samples closest to it
+            mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None and self.t1 is not None else None
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid) if (r[0] is not None and mid is not None) else 0)[:2]
+            window = "nearest samples (region shorter than the 20 ms sampling period)"
+        reasons = sorted({n for r in inside for n, v in zip(names, r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(r[3] for r in inside),
+                "window": window}
 
 
 def gpu_nvsmi_id(torch, dev):
@@ -256,11 +277,15 @@ def _timed_steps(torch, n, step, stream, sampler):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.mark_start()
     t0.record(stream)
     for i in range(n):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.mark_end()
     clocks = sampler.stop() if sampler is not None else None
     return t0.elapsed_time(t1) / 1e3, evs, clocks
 

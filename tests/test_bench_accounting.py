@@ -86,3 +86,23 @@ def test_reference_arm_line_on_the_tiny_workload(capsys):
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] in ("GB/s", "TFLOP/s")
     assert line["config"]["workload"] == "tiny" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_summary_keeps_only_the_timed_window(tmp_path):
+    """Clock samples from before or after the timed region (an idle GPU) are left out."""
+    import datetime
+    import time
+
+    p = tmp_path / "clk.csv"
+    t = time.time()
+    lines = []
+    for dt, mhz, watts, cap in [(-0.2, 2070, 180, "Not Active"), (0.01, 1940, 1370, "Active"),
+                                (0.03, 1950, 1365, "Active"), (0.3, 2070, 190, "Not Active")]:
+        ts = datetime.datetime.fromtimestamp(t + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        lines.append(f"{ts}, {mhz}, 2070, {watts}, 0x4, Not Active, Not Active, Not Active, {cap}")
+    p.write_text("\n".join(lines) + "\n")
+    c = bench.ClockSampler("0", str(p))
+    c.t0, c.t1 = t, t + 0.05
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1945.0 and s["power_w_max"] == 1370.0
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "timed region"
