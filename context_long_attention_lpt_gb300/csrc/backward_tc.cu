@@ -138,7 +138,12 @@ struct DqBarriers {
   uint64_t k_full[kKStages], k_free[kKStages];    // K(t); its dQ MMA has read it
   uint64_t v_full[kVStages], v_free[kVStages];    // V(t); its dP MMA has read it
   uint64_t s_full[2];                             // S of tile parity b ready
-  uint64_t dp_full, dp_free, ds_full;             // dP(t) ready; dP(t) read; dS(t) written
+  uint64_t dp_full, dp_free;                      // dP(t) ready; dP(t) read
+  // dS(t) written, per tile parity: every row warp arrives once per tile, and a
+  // warp may reach tile t+1 before a slower one has arrived for tile t; with one
+  // barrier per parity its arrival cannot complete tile t's phase, and tile t+2
+  // (same parity) starts only after dQ(t), which waited for all of tile t's.
+  uint64_t ds_full[2];
   uint64_t o_done, drain;
   uint32_t tmem_base;
   // Tile t's key count | (tile t+1 exists) << 16 | (tile t+2 exists) << 17, at [t & 1]:
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->s_full[b], 1);
     ptx::mbar_init(&bar->dp_full, 1);
     ptx::mbar_init(&bar->dp_free, kRowWarps);
-    ptx::mbar_init(&bar->ds_full, kRowWarps);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->ds_full[b], kRowWarps);
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has_next = (info >> 16) & 1u, has_next2 = (info >> 17) & 1u;
       if (has_next && tc::elect_one()) issue_dp(t + 1);
       __syncwarp();
-      if (!wait_all(&bar->ds_full, t & 1)) {
+      if (!wait_all(&bar->ds_full[t & 1], (t >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bar->ds_full);
+      if (lane == 0) ptx::mbar_arrive(&bar->ds_full[t & 1]);
       has2 = has3;
       has3 = has3 && ahead.next(&apos, &anv, &atok);
       ++t;

@@ -120,3 +120,21 @@ def test_backward_full_size_sampled(name):
     got_dv = torch.stack([dv[int(tc[b, p // w.block_len]), p % w.block_len, kvh].cpu() for b, kvh, p in keys])
     assert_grad_close(w.dtype, got_dk, ref_dk, f"{name} sampled dk keys")
     assert_grad_close(w.dtype, got_dv, ref_dv, f"{name} sampled dv keys")
+
+
+@pytest.mark.parametrize("name", ["decode", "shortq"])
+def test_tensor_core_backward_is_bitwise_repeatable_at_full_size(name):
+    """The tensor-core backward has no atomics: three runs give the same bits.  A hand-off race
+    between the elementwise warps and the MMA lane would show up as differing runs."""
+    w = wl.WORKLOADS[name]
+    assert K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, K.SPLITKV_BF16) == K.KERNEL_TC
+    inp, run, out, lse = run_cuda(w)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    dout = torch.randn(out.shape, generator=g, device="cuda", dtype=torch.float32).to(out.dtype)
+    first = [x.clone() for x in run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)]
+    for _ in range(2):
+        again = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
+        torch.cuda.synchronize()
+        for a_, b_ in zip(first, again):
+            assert torch.equal(a_, b_)
+    assert K.splitkv_device_status() == 0
