@@ -57,7 +57,8 @@ def test_traffic_is_used_only_for_the_source_it_was_captured_on(tmp_path, monkey
     assert bench.traffic_for("k", "w") is None
 
 
-@pytest.mark.parametrize("key", ["partial_decode/decode", "partial_tcgen05/shortq"])
+@pytest.mark.parametrize("key", ["partial_decode/decode", "partial_tcgen05/shortq", "partial_tcgen05/largest",
+                                 "partial_tcgen05/varlen"])
 def test_committed_traffic_entries_are_well_formed(key):
     """Each committed figure names an existing kernel source, its hash and a byte count.
     (An edited source makes bench.py report null until the figure is captured again.)"""
