@@ -48,6 +48,33 @@ def test_noalloc_equals_caller_buffer_path_on_two_calls_in_a_row():
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
+def test_noalloc_repeated_calls_take_no_device_memory():
+    """After the first call on the device, further calls leave torch's allocator and the
+    device's free memory where they were."""
+    w = CASES[0]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype)
+    out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device="cuda")
+    lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device="cuda")
+
+    def call():
+        K.splitkv_attention_noalloc(inp.q, inp.k_pool, inp.v_pool, inp.block_table, run.work_host, run.n_items,
+                                    run.B, run.total_q, run.max_q_len, w.block_len, w.scale, w.causal,
+                                    run.part_rows, out, lse)
+
+    call()
+    torch.cuda.synchronize()
+    free0, allocated0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(), \
+        torch.cuda.memory_reserved()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == allocated0
+    assert torch.cuda.memory_reserved() == reserved0
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
 def test_noalloc_rejects_problems_larger_than_its_array():
     w = wl.custom("shortq", q_len=512, context=131072, n_shards=64)  # 64 x 512 partial rows: > 64 MiB
     q_len, kv_len = wl.lengths(w)
