@@ -509,9 +509,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kKeySplit = 16;   // CTAs per (item, K/V head); each takes every 16th key tile
 // Warps 0-7: key threads, two per TMEM lane quarter (warp w: keys of quarter w % 4,
-// rows w / 4 * 32 .. + 31 of each 64-row tile); 8: TMA; 9: MMA.
-constexpr int kKvThreads = 320;
-constexpr int kKvProducerWarp = 8, kKvMmaWarp = 9, kKeyWarps = 8;
+// rows w / 4 * 32 .. + 31 of each 64-row tile); 8: TMA; 9: MMA; 10: sync warp,
+// which takes the copy waits off the MMA warp.
+constexpr int kKvThreads = 352;
+constexpr int kKvProducerWarp = 8, kKvMmaWarp = 9, kKvSyncWarp = 10, kKeyWarps = 8;
+// Named barriers (0 is __syncthreads).  kBarHand: the sync warp hands the MMA
+// warp each row tile's operands, both sides with bar.sync, so neither runs a
+// hand-off ahead.  kBarDs + (g & 1): the key warps hand over P^T, dS^T of row
+// tile g (bar.arrive; the MMA warp syncs).  A key warp reaches row tile g + 2
+// only after S^T(g + 2) completed, which the MMA warp issues after passing the
+// barrier of tile g, so the two parities never mix.
+constexpr int kBarHand = 1, kBarHandThreads = 64;
+constexpr int kBarDs = 2, kBarDsThreads = (kKeyWarps + 1) * 32;
 // P^T / dS^T (bf16 pairs) of rows 16 kk .. 16 kk + 15, relative to the S^T / dP^T
 // columns of the tile: rows 0-31 over columns 0-15, rows 32-63 over columns 32-47
 // (each key warp writes over the columns it has read; the other half stays intact).
@@ -530,16 +539,53 @@ struct KvBarriers {
   uint64_t kv_full;                 // K and V of the current key tile
   uint64_t qd_full[kQdStages];      // Q, dO (TMA) and L, D (producer lanes) of a row tile
   uint64_t qd_free[kQdStages];      // the row tile's dV / dK MMAs have read Q and dO
-  uint64_t s_full[2], ds_full[2];   // per row-tile parity: S^T, dP^T ready; P^T, dS^T written back
+  uint64_t s_full[2];               // per row-tile parity: S^T, dP^T ready
+  uint64_t kv_free;                 // the key tile's last S^T, dP^T completed: K, V no longer read
   uint64_t o_done;                  // the key tile's last dV / dK MMA completed
   uint64_t drain;
   uint32_t tmem_base;
-  float ld[kQdStages][2][kRowsB];   // L and D of the row tile's rows
+  // -L log2(e) and -D of the row tile's rows; -inf and 0 for rows without a
+  // gradient (past the sequence, or no visible key: L = -inf), whose P is then 0
+  alignas(16) float ld[kQdStages][2][kRowsB];
 };
 // Epilogue staging: each key warp passes 32 keys x 32 columns of dV or dK through
 // shared memory so that global stores go out as whole rows
 constexpr uint32_t kStageBytes = 4 * 32 * 32 * 4;
 constexpr size_t kKvSmem = 1024 + 2 * kTileBytes + 2 * kQdStages * kTile64 + kStageBytes + sizeof(KvBarriers);
+
+// The key threads' pass over one row tile: P^T = exp2(S^T c - L log2 e) and
+// dS^T = P^T (dP^T - D) for this thread's key and 32 rows, packed to bf16.
+// nl / nd: -L log2(e) and -D of the 32 rows.  Rows i < jlo come before the
+// key's position (causal) and get P = 0 (kMasked only).  A key past the end of
+// the tile may hold anything; its P^T, dS^T only reach its own dV, dK rows,
+// which are not stored.
+template <bool kMasked>
+__device__ __forceinline__ void key_pass(const uint32_t (&sr)[32], const uint32_t (&dp)[32], const float* nl,
+                                         const float* nd, float c, int32_t jlo, uint32_t (&pk)[16],
+                                         uint32_t (&dk2)[16]) {
+  const float2 c2 = make_float2(c, c);
+#pragma unroll
+  for (int i4 = 0; i4 < 8; ++i4) {
+    const float4 l = reinterpret_cast<const float4*>(nl)[i4];
+    const float4 dd = reinterpret_cast<const float4*>(nd)[i4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 4 * i4 + 2 * h;
+      const float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), c2,
+                                  h ? make_float2(l.z, l.w) : make_float2(l.x, l.y));
+      float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      if (kMasked) {
+        pp.x = i >= jlo ? pp.x : 0.f;
+        pp.y = i + 1 >= jlo ? pp.y : 0.f;
+      }
+      const float2 y = ptx::fadd2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
+                                  h ? make_float2(dd.z, dd.w) : make_float2(dd.x, dd.y));
+      const float2 dsv = ptx::fmul2(pp, y);
+      pk[i / 2] = pack_bf16(pp.x, pp.y);
+      dk2[i / 2] = pack_bf16(dsv.x, dsv.y);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -588,10 +634,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       ptx::mbar_init(&bar->qd_full[s], 1);
       ptx::mbar_init(&bar->qd_free[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&bar->s_full[b], 1);
-      ptx::mbar_init(&bar->ds_full[b], kKeyWarps);
-    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->s_full[b], 1);
+    ptx::mbar_init(&bar->kv_free, 1);
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
@@ -605,10 +649,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_base;
 
+  // Row tiles are numbered g = 0, 1, ... over all of this CTA's key tiles (n_rt a
+  // key tile); tile g uses ring slot g % kQdStages and the TMEM pair of parity g & 1.
   if (warp == kKvProducerWarp) {
     // ------------------------------------------------------------- producer
-    // Per key tile: K and V (after the previous key tile's MMAs are done),
-    // then every row tile's Q, dO by TMA and L, D by the warp's lanes.
+    // Per key tile: K and V, once the previous key tile's last S^T / dP^T have
+    // completed (kv_free; the dV / dK MMAs read neither), then every row tile's Q, dO by
+    // TMA and L, D by the warp's lanes.  The next key tile's K and V are
+    // prefetched into L2 when a key tile starts.
     if (lane == 0) {
       ptx::prefetch_tmap(&tmap_q);
       ptx::prefetch_tmap(&tmap_do);
@@ -616,38 +664,59 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       ptx::prefetch_tmap(&tmap_v);
     }
     TileSeq walk = tiles;
-    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
+    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0, kv_issued = 0;
     bool ok = true;
-    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
-      if (kt > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, (kt - 1) & 1))) {
+    bool have = next_mine(walk, ord, &pos0, &nv, &tok);
+    while (ok && have) {
+      const int32_t cur_tok = tok;
+      int32_t p2 = 0, nv2 = 0, tok2 = 0;
+      const bool have_next = next_mine(walk, ord, &p2, &nv2, &tok2);
+      // one kv_free phase per key tile, in order: the wait for phase kt - 1
+      // follows the load that needed phase kt - 2
+      if (kt > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_free, (kt - 1) & 1))) {
         ok = false;
         break;
       }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&bar->kv_full, 2 * kTileBytes);
-        ptx::tma_load_3d(sk, &tmap_k, 0, kvh, tok, &bar->kv_full);
-        ptx::tma_load_3d(sk + kHalfBytes, &tmap_k, 64, kvh, tok, &bar->kv_full);
-        ptx::tma_load_3d(sv, &tmap_v, 0, kvh, tok, &bar->kv_full);
-        ptx::tma_load_3d(sv + kHalfBytes, &tmap_v, 64, kvh, tok, &bar->kv_full);
+        ptx::tma_load_3d(sk, &tmap_k, 0, kvh, cur_tok, &bar->kv_full);
+        ptx::tma_load_3d(sk + kHalfBytes, &tmap_k, 64, kvh, cur_tok, &bar->kv_full);
+        ptx::tma_load_3d(sv, &tmap_v, 0, kvh, cur_tok, &bar->kv_full);
+        ptx::tma_load_3d(sv + kHalfBytes, &tmap_v, 64, kvh, cur_tok, &bar->kv_full);
+        if (have_next) {
+          ptx::tma_prefetch_3d(&tmap_k, 0, kvh, tok2);
+          ptx::tma_prefetch_3d(&tmap_k, 64, kvh, tok2);
+          ptx::tma_prefetch_3d(&tmap_v, 0, kvh, tok2);
+          ptx::tma_prefetch_3d(&tmap_v, 64, kvh, tok2);
+        }
       }
+      ++kv_issued;
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
         const int s = rt % kQdStages;
-        if (rt >= kQdStages &&
-            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_free[s], ((rt - kQdStages) / kQdStages) & 1))) {
-          ok = false;
-          break;
-        }
-        // L and D of rows r*64 .. r*64+63 (rows past the sequence: L = -inf)
-        for (int i = lane; i < kRowsB; i += 32) {
-          const int32_t row = r * kRowsB + i;
+        // -L log2(e) and -D of rows r*64 .. r*64+63 (-inf, 0 where no gradient),
+        // loaded before the slot is free so that their latency overlaps the wait
+        float nl[kRowsB / 32], nd[kRowsB / 32];
+#pragma unroll
+        for (int u = 0; u < kRowsB / 32; ++u) {
+          const int32_t row = r * kRowsB + 32 * u + lane;
           float L = -INFINITY, Dv = 0.f;
           if (row < rows) {
             const int64_t g = static_cast<int64_t>(cu_q + row / G) * a.Hq + kvh * G + row % G;
             L = __ldg(lse + g);
             Dv = __ldg(delta + g);
           }
-          bar->ld[s][0][i] = L;
-          bar->ld[s][1][i] = Dv;
+          nl[u] = L != -INFINITY ? -L * kLog2e : -INFINITY;
+          nd[u] = L != -INFINITY ? -Dv : 0.f;
+        }
+        if (rt >= kQdStages &&
+            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_free[s], ((rt - kQdStages) / kQdStages) & 1))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsB / 32; ++u) {
+          bar->ld[s][0][32 * u + lane] = nl[u];
+          bar->ld[s][1][32 * u + lane] = nd[u];
         }
         __syncwarp();
         if (lane == 0) {
@@ -660,21 +729,49 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
       }
       ++kt;
+      have = have_next;
+      tok = tok2;
     }
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     if (walk.bad_seen && lane == 0) atomicOr(a.status, 1u);
     // every copy issued has landed before shared memory is released
     if (lane == 0) {
-      if (kt > 0 && !ptx::mbar_wait(&bar->kv_full, (kt - 1) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
+      if (kv_issued > 0 && !ptx::mbar_wait(&bar->kv_full, (kv_issued - 1) & 1))
+        atomicOr(a.status, ptx::kStatusTimeout);
       for (int32_t v = max(0, rt - kQdStages); v < rt; ++v)
         if (!ptx::mbar_wait(&bar->qd_full[v % kQdStages], (v / kQdStages) & 1)) atomicOr(a.status, ptx::kStatusTimeout);
     }
+  } else if (warp == kKvSyncWarp) {
+    // ------------------------------------------------------------ sync warp
+    // Per row tile g: waits until K, V (first row tile of a key tile) and Q, dO,
+    // L, D of tile g have landed, then meets the MMA warp on kBarHand.  It cannot
+    // run ahead: each hand-off needs the MMA warp.  Once a wait has run out it
+    // stops waiting but keeps taking part in the hand-offs.
+    TileSeq walk = tiles;
+    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
+    bool ok = true;
+    while (next_mine(walk, ord, &pos0, &nv, &tok)) {
+      for (int32_t r = 0; r < n_rt; ++r, ++rt) {
+        if (ok && r == 0) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full, kt & 1));
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rt % kQdStages], (rt / kQdStages) & 1));
+        ptx::bar_sync(kBarHand, kBarHandThreads);
+      }
+      ++kt;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
   } else if (warp == kKvMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    // Row tile r uses the TMEM pair of parity b = r & 1.  S^T(r+1), dP^T(r+1)
-    // are issued before waiting for the key threads' pass over tile r, so the
-    // pipe works while they run; then dV += P^T(r) dO(r), dK += dS^T(r) Q(r).
-    // S^T(r+2) reuses tile r's columns and is issued after those MMAs (in order).
+    // Row tile g uses the TMEM pair of parity b = g & 1.  S^T(g+1), dP^T(g+1)
+    // are issued before the key threads' pass over tile g ends, so the pipe
+    // works while they run; then dV += P^T(g) dO(g), dK += dS^T(g) Q(g).
+    // S^T(g+2) reuses tile g's columns and is issued after those MMAs (in
+    // order).  At the last row tile of a key tile the dV / dK MMAs go first:
+    // the next key tile's S^T waits for its K and V, which are loaded only
+    // once this tile's last S^T has completed.  The waits are named barriers
+    // (no mbarrier wait on this warp).  The other roles keep taking part in
+    // every hand-off after a wait of theirs ran out, so this warp needs no
+    // abort test: it may then run MMAs on stale operands, which reach no
+    // output (the status word reports the timeout).
     const uint32_t idesc_s = tc::idesc_bf16_f32(kN, kRowsB, false, false);
     const uint32_t idesc_acc = tc::idesc_bf16_f32(kN, kD, false, true);
     const tc::Desc dk = tc::split(tc::smem_desc(ptx::smem_addr(sk), 16, 1024, tc::kSwizzle128B));
@@ -683,62 +780,63 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const tc::Desc ddo = tc::split(tc::smem_desc(ptx::smem_addr(sdo), 16, 1024, tc::kSwizzle128B));
     const tc::Desc dq_mn = tc::split(tc::smem_desc(ptx::smem_addr(sq), kHalf64, 1024, tc::kSwizzle128B));
     const tc::Desc ddo_mn = tc::split(tc::smem_desc(ptx::smem_addr(sdo), kHalf64, 1024, tc::kSwizzle128B));
-    // S^T, dP^T of the row tile in ring slot s into the TMEM pair b
-    auto issue_s = [&](int s, int b) {
-      const uint32_t qoff = s * (kTile64 >> 4);
+    // S^T, dP^T of row tile g (after meeting the sync warp: its operands landed);
+    // after the last row tile of a key tile, kv_free tells the producer that K
+    // and V may be overwritten
+    auto hand_and_issue_s = [&](int32_t g, bool last_of_key_tile) {
+      ptx::bar_sync(kBarHand, kBarHandThreads);
+      tc::fence_after_sync();
+      if (tc::elect_one()) {
+        const uint32_t qoff = (g % kQdStages) * (kTile64 >> 4);
+        const uint32_t b = static_cast<uint32_t>(g & 1);
 #pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_ss_fast(tmem + kColST + 64 * b, dk, kstep_off(kk), dq, qoff + kstep_off64(kk), idesc_s, kk > 0);
+        for (int kk = 0; kk < kD / 16; ++kk)
+          tc::mma_ss_fast(tmem + kColST + 64 * b, dk, kstep_off(kk), dq, qoff + kstep_off64(kk), idesc_s, kk > 0);
 #pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_ss_fast(tmem + kColDPT + 64 * b, dv, kstep_off(kk), ddo, qoff + kstep_off64(kk), idesc_s, kk > 0);
-      tc::commit(&bar->s_full[b]);
+        for (int kk = 0; kk < kD / 16; ++kk)
+          tc::mma_ss_fast(tmem + kColDPT + 64 * b, dv, kstep_off(kk), ddo, qoff + kstep_off64(kk), idesc_s, kk > 0);
+        tc::commit(&bar->s_full[b]);
+        if (last_of_key_tile) tc::commit(&bar->kv_free);
+      }
+      __syncwarp();
+    };
+    // dV, dK += row tile g (after the key warps handed over its P^T, dS^T)
+    auto sync_and_issue_acc = [&](int32_t g, bool first, bool last) {
+      const int b = g & 1;
+      ptx::bar_sync(kBarDs + b, kBarDsThreads);
+      tc::fence_after_sync();
+      if (tc::elect_one()) {
+        const uint32_t qoff = (g % kQdStages) * (kTile64 >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kRowsB / 16; ++kk)
+          tc::mma_ts_fast(tmem + kColAcc0, tmem + kColST + 64 * b + pt_col(kk), ddo_mn, qoff + kk * (2048 >> 4),
+                          idesc_acc, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kRowsB / 16; ++kk)
+          tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDPT + 64 * b + pt_col(kk), dq_mn, qoff + kk * (2048 >> 4),
+                          idesc_acc, (!first || kk > 0) ? 1u : 0u);
+        tc::commit(&bar->qd_free[g % kQdStages]);
+        if (last) tc::commit(&bar->o_done);
+      }
+      __syncwarp();
     };
     TileSeq walk = tiles;
-    int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
-    bool ok = true;
-    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->kv_full, kt & 1)) &&
-           __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rt % kQdStages], (rt / kQdStages) & 1));
-      if (!ok) break;
-      tc::fence_after_sync();
-      if (tc::elect_one()) issue_s(rt % kQdStages, rt & 1);
-      __syncwarp();
+    int32_t ord = 0, pos0, nv, tok, rt = 0;
+    bool have = next_mine(walk, ord, &pos0, &nv, &tok);
+    if (have) hand_and_issue_s(0, n_rt == 1);
+    while (have) {
+      const bool have_next = next_mine(walk, ord, &pos0, &nv, &tok);
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
-        const int s = rt % kQdStages, b = rt & 1;
         if (r + 1 < n_rt) {
-          const int32_t rn = rt + 1;
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[rn % kQdStages], (rn / kQdStages) & 1))) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          if (tc::elect_one()) issue_s(rn % kQdStages, rn & 1);
-          __syncwarp();
+          hand_and_issue_s(rt + 1, r + 2 == n_rt);
+          sync_and_issue_acc(rt, r == 0, false);
+        } else {
+          sync_and_issue_acc(rt, r == 0, true);
+          if (have_next) hand_and_issue_s(rt + 1, n_rt == 1);
         }
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->ds_full[b], (rt >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (tc::elect_one()) {
-          const uint32_t qoff = s * (kTile64 >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kRowsB / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc0, tmem + kColST + 64 * b + pt_col(kk), ddo_mn, qoff + kk * (2048 >> 4),
-                            idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kRowsB / 16; ++kk)
-            tc::mma_ts_fast(tmem + kColAcc1, tmem + kColDPT + 64 * b + pt_col(kk), dq_mn, qoff + kk * (2048 >> 4),
-                            idesc_acc, (r > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(&bar->qd_free[s]);
-          if (r == n_rt - 1) tc::commit(&bar->o_done);
-        }
-        __syncwarp();
       }
-      ++kt;
+      have = have_next;
     }
-    if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     if (tc::elect_one()) tc::commit(&bar->drain);
     __syncwarp();
     if (!ptx::mbar_wait(&bar->drain, 0) && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
@@ -751,62 +849,53 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     TileSeq walk = tiles;
     int32_t ord = 0, pos0, nv, tok, kt = 0, rt = 0;
     bool ok = true;
-    while (ok && next_mine(walk, ord, &pos0, &nv, &tok)) {
-      const bool key_valid = k < nv;
+    while (next_mine(walk, ord, &pos0, &nv, &tok)) {
       // causal: the row (token t, head) sees this key iff t >= pos - (kv_len - q_len)
-      const int32_t t_first = a.causal ? max(0, pos0 + k - (kv_len - q_len)) : 0;
+      const int32_t t_first = a.causal ? min(q_len, max(0, pos0 + k - (kv_len - q_len))) : 0;
       for (int32_t r = 0; r < n_rt; ++r, ++rt) {
         const int s = rt % kQdStages, b = rt & 1;
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kQdStages) & 1)) ||
-            !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[b], (rt >> 1) & 1))) {
-          ok = false;
-          break;
+        if (ok)
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->qd_full[s], (rt / kQdStages) & 1)) &&
+               __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[b], (rt >> 1) & 1));
+        if (!ok) {
+          // no more TMEM work, but every hand-off still takes place (bar.sync
+          // keeps this warp in step with the MMA warp)
+          ptx::bar_sync(kBarDs + b, kBarDsThreads);
+          continue;
         }
         tc::fence_after_sync();
-        // rows j of the tile this key contributes to: [jmin, jmax)
-        const int32_t jmin = key_valid ? max(0, t_first * G - r * kRowsB) : kRowsB;
-        const int32_t jmax = min(kRowsB, rows - r * kRowsB);
-        const float* Ls = bar->ld[s][0] + 32 * hh;
-        const float* Ds = bar->ld[s][1] + 32 * hh;
+        // this thread's rows are 32 hh + i of the tile; causal: those below
+        // t_first * G - r * 64 come before the key
+        const int32_t jlo = t_first * G - r * kRowsB - 32 * hh;
+        const float* nl = bar->ld[s][0] + 32 * hh;
+        const float* nd = bar->ld[s][1] + 32 * hh;
         const uint32_t st_col = kColST + 64 * b + 32 * hh, dpt_col = kColDPT + 64 * b + 32 * hh;
         uint32_t sr[32], dp[32], pk[16], dk2[16];
         tc::tmem_ld32(lane_addr + st_col, sr);
         tc::tmem_ld32(lane_addr + dpt_col, dp);
         tc::tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = 32 * hh + i + e;
-            const float Lj = Ls[i + e];
-            const bool on = j >= jmin && j < jmax && Lj != -INFINITY;
-            const float pj = fast_exp2(__uint_as_float(sr[i + e]) * c - Lj * kLog2e);
-            p[e] = on ? pj : 0.f;
-            ds[e] = on ? pj * (__uint_as_float(dp[i + e]) - Ds[i + e]) : 0.f;
-          }
-          pk[i / 2] = pack_bf16(p[0], p[1]);
-          dk2[i / 2] = pack_bf16(ds[0], ds[1]);
-        }
+        if (__all_sync(0xffffffffu, jlo <= 0))
+          key_pass<false>(sr, dp, nl, nd, c, jlo, pk, dk2);
+        else
+          key_pass<true>(sr, dp, nl, nd, c, jlo, pk, dk2);
         // P^T over this half's first 16 S^T columns, dS^T over its first 16 dP^T
         // columns: both already read, and the other half's columns stay intact
         tc::tmem_st16(lane_addr + st_col, pk);
         tc::tmem_st16(lane_addr + dpt_col, dk2);
         tc::tmem_st_wait();
         tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar->ds_full[b]);
+        ptx::bar_arrive(kBarDs + b, kBarDsThreads);
       }
-      if (!ok) break;
       // epilogue: this key's dV and dK = scale * sum dS^T Q, by the warps of the
       // first half (one per lane quarter); the others go on to the next key tile
       if (hh == 1) {
         ++kt;
         continue;
       }
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, kt & 1))) {
-        ok = false;
-        break;
+      if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, kt & 1));
+      if (!ok) {
+        ++kt;
+        continue;
       }
       tc::fence_after_sync();
       // Each chunk of 32 columns goes through this warp's 32 x 32 staging block

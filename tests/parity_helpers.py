@@ -44,6 +44,9 @@ SMALL = {
     # causal queries longer than the context, one block per shard: the first query rows see
     # none of the last blocks, so many (item, head, row tile) units have no key tile at all
     "causal_empty_units": wl.custom("shortq", q_len=600, context=100, block_len=128, n_shards=6),
+    # one 64-row tile per sequence and ~12 key tiles per dK/dV CTA: K and V are reloaded
+    # after every row tile
+    "many_key_tiles": wl.custom("shortq", q_len=16, context=24000, block_len=128, n_shards=1),
 }
 
 

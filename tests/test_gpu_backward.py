@@ -45,7 +45,7 @@ def _check_every_element(w, inp, out, lse, dout, dq, dk, dv, what):
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_small", "shortq_small", "varlen_small", "noncausal_multi_q",
-                                  "bf16_d64", "largest_small", "causal_empty_units"])
+                                  "bf16_d64", "largest_small", "causal_empty_units", "many_key_tiles"])
 def test_backward_matches_oracle(name):
     w = SMALL[name]
     inp, run, out, lse = run_cuda(w)
@@ -122,17 +122,24 @@ def test_backward_full_size_sampled(name):
     assert_grad_close(w.dtype, got_dv, ref_dv, f"{name} sampled dv keys")
 
 
-@pytest.mark.parametrize("name", ["decode", "shortq"])
+REPEAT_CASES = {name: wl.WORKLOADS[name] for name in ("decode", "shortq", "largest", "varlen")}
+# three 64-row tiles per sequence and ~49 key tiles per dK/dV CTA: K and V are reloaded
+# every third row tile while the next loads are in flight
+REPEAT_CASES["reload_kv"] = wl.custom("shortq", q_len=48, context=200000, block_len=1024, n_shards=2)
+
+
+@pytest.mark.parametrize("name", list(REPEAT_CASES))
 def test_tensor_core_backward_is_bitwise_repeatable_at_full_size(name):
-    """The tensor-core backward has no atomics: three runs give the same bits.  A hand-off race
-    between the elementwise warps and the MMA lane would show up as differing runs."""
-    w = wl.WORKLOADS[name]
+    """The tensor-core backward has no atomics: repeated runs give the same bits.  A hand-off
+    race between the elementwise warps and the MMA lane, or a K/V reload over a tile still in
+    use, would show up as differing runs."""
+    w = REPEAT_CASES[name]
     assert K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, K.SPLITKV_BF16) == K.KERNEL_TC
     inp, run, out, lse = run_cuda(w)
     g = torch.Generator(device="cuda").manual_seed(31)
     dout = torch.randn(out.shape, generator=g, device="cuda", dtype=torch.float32).to(out.dtype)
     first = [x.clone() for x in run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)]
-    for _ in range(2):
+    for _ in range(4):
         again = run.backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale, out, lse, dout)
         torch.cuda.synchronize()
         for a_, b_ in zip(first, again):
