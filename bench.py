@@ -47,9 +47,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="largest")
-    ap.add_argument("--per-workload", default="decode,shortq,varlen",
+    ap.add_argument("--per-workload", default="decode,shortq,varlen,specdec",
                     help="forward workloads also timed in the same run (comma list, '' for none)")
-    ap.add_argument("--per-backward", default="shortq",
+    ap.add_argument("--per-backward", default="shortq,largest,varlen",
                     help="workloads whose backward pass is also timed in the same run ('' for none)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "decode", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -47,6 +47,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // quarter w % 4, key columns w / 4 * 64 .. + 63 of each key tile); 8: TMA; 9: MMA
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kRowWarps = 8;
+// Named barriers of the dQ kernel (0 is __syncthreads), between the row warps
+// (bar.arrive) and the MMA warp (bar.sync): kBarDpFree, dP(t) read; kBarDsQ +
+// (t & 1), dS(t) written.  A row warp reaches dP(t+1) only after dP(t+1) was
+// issued, which follows the MMA warp's pass of kBarDpFree for tile t, and
+// dS(t+2) only after S(t+2), which follows its pass of kBarDsQ for tile t: no
+// generation mixes arrivals of two tiles.
+constexpr int kBarDpFree = 1, kBarDsQ = 2, kBarDqThreads = (kRowWarps + 1) * 32;
 // dS (bf16 pairs) of keys 16 kk .. 16 kk + 15, relative to the S columns of the
 // tile: keys 0-63 over columns 0-31, keys 64-127 over columns 64-95 (each row
 // warp writes over the columns it has read; the other half stays intact).
@@ -138,12 +145,7 @@ struct DqBarriers {
   uint64_t k_full[kKStages], k_free[kKStages];    // K(t); its dQ MMA has read it
   uint64_t v_full[kVStages], v_free[kVStages];    // V(t); its dP MMA has read it
   uint64_t s_full[2];                             // S of tile parity b ready
-  uint64_t dp_full, dp_free;                      // dP(t) ready; dP(t) read
-  // dS(t) written, per tile parity: every row warp arrives once per tile, and a
-  // warp may reach tile t+1 before a slower one has arrived for tile t; with one
-  // barrier per parity its arrival cannot complete tile t's phase, and tile t+2
-  // (same parity) starts only after dQ(t), which waited for all of tile t's.
-  uint64_t ds_full[2];
+  uint64_t dp_full;                               // dP(t) ready
   uint64_t o_done, drain;
   uint32_t tmem_base;
   // Tile t's key count | (tile t+1 exists) << 16 | (tile t+2 exists) << 17, at [t & 1]:
@@ -204,8 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->s_full[b], 1);
     ptx::mbar_init(&bar->dp_full, 1);
-    ptx::mbar_init(&bar->dp_free, kRowWarps);
-    for (int b = 0; b < 2; ++b) ptx::mbar_init(&bar->ds_full[b], kRowWarps);
     ptx::mbar_init(&bar->o_done, 1);
     ptx::mbar_init(&bar->drain, 1);
     ptx::fence_mbar_init();
@@ -298,43 +298,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* b, uint32_t parity) { return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity)); };
     int32_t pos0, tok, nv0 = 0, nv1 = 0;
     TileSeq walk = tiles;
+    // The tile walk does not depend on the waits: this warp takes part in one
+    // kBarDpFree and one kBarDsQ hand-off per tile whatever happens (after a
+    // timeout its MMAs may read stale operands; the status word reports it).
     bool ok = wait_all(&bar->qd_full, 0);
-    bool has_cur = ok && walk.next(&pos0, &nv0, &tok);
+    bool has_cur = walk.next(&pos0, &nv0, &tok);
     const bool has_one = has_cur && walk.next(&pos0, &nv1, &tok);
     if (has_cur) {
-      ok = wait_all(&bar->k_full[0], 0) && wait_all(&bar->v_full[0], 0);
+      ok = wait_all(&bar->k_full[0], 0) && wait_all(&bar->v_full[0], 0) && ok;
       tc::fence_after_sync();
-      if (ok && tc::elect_one()) {
+      if (tc::elect_one()) {
         issue_s(0);
         issue_dp(0);
       }
       __syncwarp();
-      if (ok && has_one) {
-        ok = wait_all(&bar->k_full[1 % kKStages], 0);
+      if (has_one) {
+        ok = wait_all(&bar->k_full[1 % kKStages], 0) && ok;
         tc::fence_after_sync();
-        if (ok && tc::elect_one()) issue_s(1);
+        if (tc::elect_one()) issue_s(1);
         __syncwarp();
       }
     }
     int32_t t = 0;
-    while (has_cur && ok) {
-      if (!wait_all(&bar->dp_free, t & 1)) {
-        ok = false;
-        break;
-      }
+    while (has_cur) {
+      ptx::bar_sync(kBarDpFree, kBarDqThreads);  // dP(t) read; V(t+1) landed; tinfo
       tc::fence_after_sync();
       const uint32_t info = bar->tinfo[t & 1];
       const int32_t nv_cur = static_cast<int32_t>(info & 0xffffu);
       const bool has_next = (info >> 16) & 1u, has_next2 = (info >> 17) & 1u;
       if (has_next && tc::elect_one()) issue_dp(t + 1);
       __syncwarp();
-      if (!wait_all(&bar->ds_full[t & 1], (t >> 1) & 1)) {
-        ok = false;
-        break;
-      }
+      ptx::bar_sync(kBarDsQ + (t & 1), kBarDqThreads);  // dS(t) written; K(t+2) landed
       tc::fence_after_sync();
       const int ks = t % kKStages;
-      const int ksteps = (nv_cur + 15) >> 4;
+      const int ksteps = (min(max(nv_cur, 0), kN) + 15) >> 4;
       if (nv_cur < ksteps * 16) {
         // K rows of keys past the end inside the last 16-key step: zero (their dS
         // is 0, but the pool slot may hold anything); S(t) has read them already
@@ -381,16 +378,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool has2 = has1 && ahead.next(&apos, &anv, &atok);  // tile 1 exists
     bool has3 = has2 && ahead.next(&apos, &anv, &atok);  // tile 2 exists
     bool ok = true;
-    while (ok && walk.next(&pos0, &nvalid, &tok)) {
+    const float2 c2 = make_float2(c, c), nlc2 = make_float2(-lc, -lc), nd2 = make_float2(-Dr, -Dr);
+    while (walk.next(&pos0, &nvalid, &tok)) {
       const bool has_next = has2, has_next2 = has3;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1)) ||
-          !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->dp_full, t & 1))) {
-        ok = false;
-        break;
+      // tile t's key count and whether tiles t+1, t+2 exist, for the MMA warp
+      const uint32_t info = static_cast<uint32_t>(nvalid) | (has_next ? 1u << 16 : 0u) | (has_next2 ? 1u << 17 : 0u);
+      if (ok)
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[t & 1], (t >> 1) & 1)) &&
+             __all_sync(0xffffffffu, ptx::mbar_wait(&bar->dp_full, t & 1));
+      if (!ok) {
+        // a wait ran out: no more TMEM work, but both hand-offs of every tile
+        // still take place (bar.sync keeps this warp in step with the MMA warp)
+        if (warp == 0 && lane == 0) bar->tinfo[t & 1] = info;
+        __syncwarp();
+        ptx::bar_sync(kBarDpFree, kBarDqThreads);
+        ptx::bar_sync(kBarDsQ + (t & 1), kBarDqThreads);
+        has2 = has3;
+        has3 = has3 && ahead.next(&apos, &anv, &atok);
+        ++t;
+        continue;
       }
       tc::fence_after_sync();
       // keys [0, lim) of this warp's 64 columns are seen
       const int32_t lim = (live ? min(nvalid, my_vis - pos0) : 0) - 64 * hh;
+      const bool whole = __all_sync(0xffffffffu, lim >= 64);  // no masking in this warp
       const uint32_t s_col = kColS0 + 128 * (t & 1) + 64 * hh, dp_col = kColDPq + 64 * hh;
       // this warp's 64 columns, 32 at a time; dS (bf16) over the first 32 S
       // columns of its half, all already read when written
@@ -402,27 +413,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_wait();
         if (q == 1) {  // all of this warp's dP(t) is in registers: the next dP may be issued
           if (warp == 0) {
-            if (lane == 0)
-              bar->tinfo[t & 1] = static_cast<uint32_t>(nvalid) | (has_next ? 1u << 16 : 0u) |
-                                  (has_next2 ? 1u << 17 : 0u);
+            if (lane == 0) bar->tinfo[t & 1] = info;
             if (has_next && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->v_full[(t + 1) % kVStages],
                                                                     ((t + 1) / kVStages) & 1)))
               ok = false;
           }
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bar->dp_free);
+          ptx::bar_arrive(kBarDpFree, kBarDqThreads);
         }
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int j = 32 * q + i;
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float p = fast_exp2(__uint_as_float(sr[i + e]) * c - lc);
-            ds[e] = j + e < lim ? p * (__uint_as_float(dp[i + e]) - Dr) : 0.f;
+          const float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), c2, nlc2);
+          const float2 y = ptx::fadd2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
+          float2 ds = ptx::fmul2(make_float2(fast_exp2(x.x), fast_exp2(x.y)), y);
+          if (!whole) {
+            const int j = 32 * q + i;
+            ds.x = j < lim ? ds.x : 0.f;
+            ds.y = j + 1 < lim ? ds.y : 0.f;
           }
-          pk[i / 2] = pack_bf16(ds[0], ds[1]);
+          pk[i / 2] = pack_bf16(ds.x, ds.y);
         }
         tc::tmem_st16(lane_addr + s_col + 16 * q, pk);
       }
@@ -432,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bar->ds_full[t & 1]);
+      ptx::bar_arrive(kBarDsQ + (t & 1), kBarDqThreads);
       has2 = has3;
       has3 = has3 && ahead.next(&apos, &anv, &atok);
       ++t;

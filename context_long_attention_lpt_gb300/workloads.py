@@ -4,10 +4,12 @@ This module only draws inputs.  It holds none of the method's arithmetic (no
 costs, plans, scores or merges), so both the CUDA path and the CPU oracle can
 be fed from it without sharing any computation.
 
-The five workloads are the short-query / long-context shapes the Split-KV card
-targets ("very short queries and very long contexts", card intro): a tiny fp32
-exactness case, batched decode, a 512-token query over a 128K context, a
-variable-length batch, and a 256-token query over a 1M context.
+The five main workloads are the short-query / long-context shapes the Split-KV
+card targets ("very short queries and very long contexts", card intro): a tiny
+fp32 exactness case, batched decode, a 512-token query over a 128K context, a
+variable-length batch, and a 256-token query over a 1M context.  A sixth,
+``specdec``, sits between decode and the tile-filling shapes: four query tokens
+per sequence (16 query rows per K/V head), as in speculative decoding.
 
 Recipe (seed = workload index unless overridden):
 * lengths: ``numpy.random.default_rng(seed)``; variable-length contexts are
@@ -85,6 +87,11 @@ WORKLOADS = {
         varlen=True, seed=4,
         description="16 seqs, context log-U[4096,131072], Lq U[64,1024] causal tail, Hq=32 Hkv=8 d=128 "
                     "bf16, block_len=1024, S=64"),
+    "specdec": Workload(
+        "specdec", B=8, Hq=32, Hkv=8, d=128, block_len=256, n_shards=16, causal=True, dtype="bf16",
+        q_len=4, context=32768, seed=6,
+        description="B=8 Hq=32 Hkv=8 d=128 Lq=4 causal tail after Lkv=32768 bf16 (16 query rows per "
+                    "K/V head), paged block_len=256, S=16"),
     "largest": Workload(
         "largest", B=1, Hq=32, Hkv=8, d=128, block_len=2048, n_shards=64, causal=True, dtype="bf16",
         q_len=256, context=1048576, q_scale=2.0, seed=5,

@@ -46,6 +46,7 @@ SMALL = {
     "causal_empty_units": wl.custom("shortq", q_len=600, context=100, block_len=128, n_shards=6),
     # one 64-row tile per sequence and ~12 key tiles per dK/dV CTA: K and V are reloaded
     # after every row tile
+    "specdec_small": wl.custom("specdec", B=3, context=3000, n_shards=5),
     "many_key_tiles": wl.custom("shortq", q_len=16, context=24000, block_len=128, n_shards=1),
 }
 

@@ -81,7 +81,7 @@ def test_partials_match_oracle_partials(name, kernel):
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_full_size_workloads_sampled_rows(name):
-    """The five workloads at full size, auto kernel (what the benchmark runs), sampled rows."""
+    """Every workload at full size, auto kernel (what the benchmark runs), sampled rows."""
     w = wl.WORKLOADS[name]
     inp, run, out, lse = run_cuda(w, kernel=K.KERNEL_AUTO)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
