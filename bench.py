@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
                     help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
                          "reduction completion model (splitkv_plan_dcp)")
+    ap.add_argument("--tail-pieces", type=int, default=0,
+                    help="cut the items of the last partial wave of CTAs into this many pieces "
+                         "(splitkv_build_work_tail; 0: no cut)")
     ap.add_argument("--item-blocks", type=int, default=0,
                     help="cut work items into runs of at most this many blocks (0: one item per shard and "
                          "sequence)")
@@ -308,15 +311,23 @@ def measure_forward(args, dctx, name, dev, headline=False):
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
                            inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
                            planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma,
-                           item_blocks=args.item_blocks if headline else 0)
+                           item_blocks=args.item_blocks if headline else 0,
+                           tail_pieces=args.tail_pieces if headline else 0)
     fused_one_launch = run.fused and run.fuses_in_one_launch()
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
     acc = workload_accounting(w, inp.q_len, inp.kv_len, run.block_cost, run.part_rows)
     stream = torch.cuda.current_stream()
 
+    # One step = the device calls on the plan made at the end of the previous step, then the
+    # next step's plan (block costs, LPT, work lists, descriptor upload).  Planning after the
+    # launches lets the host work overlap the kernels, so the events around each launch time
+    # the kernel and not a device waiting for the host; every step still plans once.  The
+    # upload goes on its own stream into the descriptor buffer the running step does not read.
+    upload_stream = torch.cuda.Stream()
+    run.plan(stream=upload_stream)
+
     def step(ev=None):
-        run.plan()
         if ev is not None:
             ev[0].record(stream)
         if run.fused:
@@ -324,13 +335,14 @@ def measure_forward(args, dctx, name, dev, headline=False):
             if ev is not None:
                 ev[1].record(stream)
                 ev[2].record(stream)
-            return
-        run.partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
-        if ev is not None:
-            ev[1].record(stream)
-        run.merge(out, lse)
-        if ev is not None:
-            ev[2].record(stream)
+        else:
+            run.partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+            if ev is not None:
+                ev[1].record(stream)
+            run.merge(out, lse)
+            if ev is not None:
+                ev[2].record(stream)
+        run.plan(stream=upload_stream)
 
     for _ in range(args.warmup):
         step()

@@ -53,6 +53,36 @@ extern "C" int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t b
   return pick_kernel(a, SPLITKV_KERNEL_AUTO);
 }
 
+extern "C" int splitkv_partial_slots(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t max_q_len,
+                                     int32_t dtype, int32_t kernel, int32_t* units_per_item) {
+  splitkv::PartialArgs a{};
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.block_len = block_len;
+  a.max_q_len = max_q_len;
+  a.dtype = dtype;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_q_len <= 0) return fail(SPLITKV_ERR_INVALID, "bad shape");
+  if (!units_per_item) return fail(SPLITKV_ERR_INVALID, "splitkv_partial_slots: null argument");
+  const int k = pick_kernel(a, kernel);
+  int blocks = 0, st = SPLITKV_OK;
+  if (k == SPLITKV_KERNEL_DECODE && splitkv::decode_supports(a)) {
+    *units_per_item = Hkv;
+    st = splitkv::decode_blocks_per_sm(a, &blocks);
+  } else if (k == SPLITKV_KERNEL_TC && splitkv::tc_supports(a)) {
+    st = splitkv::tc_blocks_per_sm(a, &blocks, units_per_item);
+  } else {
+    return fail(SPLITKV_ERR_UNSUPPORTED, "splitkv_partial_slots: only the decode and tensor-core kernels");
+  }
+  if (st != SPLITKV_OK) return st;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  splitkv::clear_error();
+  return blocks * sms;
+}
+
 extern "C" int splitkv_backward_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t dtype) {
   splitkv::PartialArgs a{};
   a.Hq = Hq;

@@ -47,6 +47,11 @@ cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);
 int launch_partial_decode(const PartialArgs& a, cudaStream_t stream);
 int launch_partial_tc(const PartialArgs& a, cudaStream_t stream);
 
+// CTAs of the specialised kernels one SM keeps resident (and, for the tensor-core
+// kernel, CTAs launched per work item); SPLITKV_* status.
+int decode_blocks_per_sm(const PartialArgs& a, int* blocks);
+int tc_blocks_per_sm(const PartialArgs& a, int* blocks, int32_t* units_per_item);
+
 // Shape limits of the specialised kernels (checked before launching them).
 bool decode_supports(const PartialArgs& a);
 bool decode_fuses(const PartialArgs& a);  // the decode kernel can merge in the same launch

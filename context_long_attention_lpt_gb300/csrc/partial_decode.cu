@@ -415,6 +415,24 @@ bool decode_supports(const PartialArgs& a) {
          static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
 }
 
+int decode_blocks_per_sm(const PartialArgs& a, int* blocks) {
+  const int64_t rows = static_cast<int64_t>(a.max_q_len) * (a.Hq / a.Hkv);
+  cudaError_t e;
+  if (rows <= 4) {
+    e = cudaFuncSetAttribute(partial_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, partial_decode_kernel<4>, kThreads, kSmemBytes);
+  } else {
+    e = cudaFuncSetAttribute(partial_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, partial_decode_kernel<8>, kThreads, kSmemBytes);
+  }
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "decode occupancy: %s", cudaGetErrorString(e));
+  return SPLITKV_OK;
+}
+
 int launch_partial_decode(const PartialArgs& a, cudaStream_t stream) {
   const int64_t grid = static_cast<int64_t>(a.n_items) * a.Hkv;
   if (grid == 0) return SPLITKV_OK;

@@ -656,6 +656,15 @@ bool tc_supports(const PartialArgs& a) {
          static_cast<int64_t>(a.n_pool_blocks) * a.block_len < (1ll << 31);
 }
 
+int tc_blocks_per_sm(const PartialArgs& a, int* blocks, int32_t* units_per_item) {
+  *units_per_item = (a.max_q_len * (a.Hq / a.Hkv) + kM - 1) / kM * a.Hkv;
+  cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, partial_tc_kernel, kThreads, kSmemBytes);
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "tc occupancy: %s", cudaGetErrorString(e));
+  return SPLITKV_OK;
+}
+
 int launch_partial_tc(const PartialArgs& a, cudaStream_t stream) {
   const int32_t G = a.Hq / a.Hkv;
   const int32_t units = (a.max_q_len * G + kM - 1) / kM;

@@ -215,12 +215,22 @@ extern "C" int64_t splitkv_work_words(int64_t n_blocks, int32_t B) {
 
 namespace {
 
-// Work lists of a plan; max_item_blocks > 0 cuts every (shard, sequence) run of
-// blocks into items of at most that many blocks (0: one item per pair).
+// How a plan's (shard, sequence) runs of blocks become work items.
+//   max_item_blocks > 0: every run is cut into items of at most that many blocks.
+//   tail: with units_per_item CTAs launched per item and `slots` CTAs resident at
+//   once, the items whose CTAs fall in the last, partly filled wave (launch order)
+//   are each cut into up to `pieces` runs of consecutive blocks.
+struct ItemCut {
+  int32_t max_item_blocks = 0;
+  int32_t units_per_item = 0, slots = 0, pieces = 0;
+};
+
+// Work lists of a plan, with items cut as `cut` says (default: one item per pair).
 int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
                const int64_t* block_cost, const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
-               int32_t max_item_blocks, int32_t* work, int64_t work_words, int32_t* n_items_out,
+               const ItemCut& cut, int32_t* work, int64_t work_words, int32_t* n_items_out,
                int64_t* part_rows_out) {
+  const int32_t max_item_blocks = cut.max_item_blocks;
   using namespace splitkv;
   int st = 0;
   if (!check_lengths(q_len, kv_len, B, block_len, &st)) return st;
@@ -228,6 +238,8 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
     return fail(SPLITKV_ERR_INVALID, "splitkv_build_work: null argument");
   if (n_shards <= 0) return fail(SPLITKV_ERR_INVALID, "n_shards must be positive");
   if (max_item_blocks < 0) return fail(SPLITKV_ERR_INVALID, "max_item_blocks must be >= 0");
+  if (cut.units_per_item < 0 || cut.slots < 0 || cut.pieces < 0)
+    return fail(SPLITKV_ERR_INVALID, "units_per_item, slots and pieces must be >= 0");
   const int64_t need = splitkv_work_words(n_blocks, B);
   if (need < 0) return static_cast<int>(need);
   if (work_words < need)
@@ -286,6 +298,34 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
   std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
     return items[x].cost > items[y].cost;
   });
+  // Tail cut: the items of the last partial wave, in launch order, each become up
+  // to `pieces` items of consecutive blocks, launched last (piece order kept).
+  const int64_t units = static_cast<int64_t>(items.size()) * cut.units_per_item;
+  if (cut.units_per_item > 0 && cut.slots > 0 && cut.pieces > 1 && units > cut.slots && units % cut.slots != 0) {
+    const int64_t tail = (units % cut.slots + cut.units_per_item - 1) / cut.units_per_item;
+    const int64_t n0 = static_cast<int64_t>(items.size());
+    std::vector<int64_t> rank(static_cast<size_t>(n0));
+    for (int64_t r = 0; r < n0; ++r) rank[order[r]] = r;
+    std::vector<Item> cut_items;
+    std::vector<int64_t> key;  // launch position: parent rank * pieces + piece
+    for (int64_t i = 0; i < n0; ++i) {
+      const Item& it = items[i];
+      const int64_t p = rank[i] >= n0 - tail ? std::min<int64_t>(cut.pieces, it.count) : 1;
+      int64_t first = it.first;
+      for (int64_t k = 0; k < p; ++k) {
+        const int64_t cnt = it.count / p + (k < it.count % p ? 1 : 0);
+        Item piece{it.shard, it.seq, first, cnt, 0};
+        for (int64_t j = first; j < first + cnt; ++j) piece.cost += block_cost[idx[j]];
+        cut_items.push_back(piece);
+        key.push_back(rank[i] * cut.pieces + k);
+        first += cnt;
+      }
+    }
+    items.swap(cut_items);
+    order.resize(items.size());
+    for (size_t i = 0; i < items.size(); ++i) order[i] = static_cast<int32_t>(i);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return key[x] < key[y]; });
+  }
 
   const int32_t n_items = static_cast<int32_t>(items.size());
   const int64_t off_seq = kHeaderWords;
@@ -364,7 +404,7 @@ extern "C" int splitkv_build_work(const int32_t* q_len, const int32_t* kv_len, i
                                   const int32_t* shard_of_block, int64_t n_blocks,
                                   int32_t n_shards, int32_t* work, int64_t work_words,
                                   int32_t* n_items_out, int64_t* part_rows_out) {
-  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, 0, work,
+  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, ItemCut{}, work,
                     work_words, n_items_out, part_rows_out);
 }
 
@@ -373,8 +413,23 @@ extern "C" int splitkv_build_work_split(const int32_t* q_len, const int32_t* kv_
                                         const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
                                         int32_t max_item_blocks, int32_t* work, int64_t work_words,
                                         int32_t* n_items_out, int64_t* part_rows_out) {
-  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, max_item_blocks,
-                    work, work_words, n_items_out, part_rows_out);
+  ItemCut cut;
+  cut.max_item_blocks = max_item_blocks;
+  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, cut, work,
+                    work_words, n_items_out, part_rows_out);
+}
+
+extern "C" int splitkv_build_work_tail(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                                       int32_t block_len, const int64_t* block_cost,
+                                       const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+                                       int32_t units_per_item, int32_t slots, int32_t pieces, int32_t* work,
+                                       int64_t work_words, int32_t* n_items_out, int64_t* part_rows_out) {
+  ItemCut cut;
+  cut.units_per_item = units_per_item;
+  cut.slots = slots;
+  cut.pieces = pieces;
+  return build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, cut, work,
+                    work_words, n_items_out, part_rows_out);
 }
 
 extern "C" int splitkv_plan_dcp(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,

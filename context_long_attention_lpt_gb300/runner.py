@@ -11,11 +11,12 @@ allocated with torch and reused across calls of the same shape.  It computes
 nothing itself.
 
 Streams: ``plan(stream=s)`` uploads the work descriptor on ``s`` (default: the
-current stream).  A device call on another stream first waits for that upload,
-and the next upload waits for the last device call that read the descriptor,
-so plans and calls may use different streams.  The partial buffers are shared
-by ``partial`` and ``merge``: calls of one batch on different streams are
-ordered by the caller, as with any stream API.
+current stream) into one of two device buffers, used in turn.  A device call on
+another stream first waits for that upload, and an upload into a buffer waits
+for the last device call that read it, so plans and calls may use different
+streams: planning batch i+1 on a copy stream overlaps batch i's kernels.  The
+partial buffers are shared by ``partial`` and ``merge``: calls of one batch on
+different streams are ordered by the caller, as with any stream API.
 """
 
 import numpy as np
@@ -27,7 +28,7 @@ from . import splitkv as _k
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
                  device="cuda", kernel=_k.KERNEL_AUTO, fused=False, planner="lpt", dcp_alpha=1.0,
-                 dcp_beta=0.0, dcp_gamma=0.0, item_blocks=0):
+                 dcp_beta=0.0, dcp_gamma=0.0, item_blocks=0, tail_pieces=0, tail_slots=None):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -45,6 +46,9 @@ class SplitKVAttention:
         self.dcp_alpha, self.dcp_beta, self.dcp_gamma = float(dcp_alpha), float(dcp_beta), float(dcp_gamma)
         self.n_shards_used = self.n_shards
         self.item_blocks = int(item_blocks)  # > 0: work items of at most this many blocks
+        self.tail_pieces = int(tail_pieces)  # > 1: the last partial wave's items cut into this many
+        self.tail_slots = tail_slots  # resident CTAs assumed by the cut (None: the library's count)
+        self._slots = None
         self._tickets = None
         self._grad_pools = None
         self.total_q = sum(self.q_len)
@@ -53,13 +57,16 @@ class SplitKVAttention:
         self._kv_len_np = np.asarray(self.kv_len, dtype=np.int32)
         # pinned staging buffers for the work list, used in turn, so planning the
         # next batches on the host runs up to len(ring) uploads ahead of the device
-        self._ring = [[None, None] for _ in range(3)]  # [pinned buffer, upload-done event]
+        # (a few KB each; eight steps absorb a host stall of about a millisecond on
+        # the shortest workloads)
+        self._ring = [[None, None] for _ in range(8)]  # [pinned buffer, upload-done event]
         self._ring_next = 0
-        self._work_dev = None
+        self._work_dev = [None, None]  # device descriptors, used in turn
+        self._cur = 1                  # the buffer the device calls read (flipped by each plan)
         self._o_part = None
         self._lse_part = None
-        self._upload = None    # (event, stream) of the last work upload
-        self._last_use = None  # event after the last device call that read the work buffer
+        self._upload = None            # (event, stream) of the last work upload
+        self._last_use = [None, None]  # per buffer: event after the last device call that read it
         self.plan()
 
     # host steps -------------------------------------------------------------
@@ -74,7 +81,21 @@ class SplitKVAttention:
             self.n_shards_used, self.shard_of_block, self.shard_load, self.modeled_time = _k.splitkv_plan_dcp(
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
                 self.dcp_beta, self.dcp_gamma)
-        if self.item_blocks > 0:
+        if self.tail_pieces > 1 and self.item_blocks > 0:
+            raise ValueError("tail_pieces and item_blocks are exclusive")
+        if self.tail_pieces > 1:
+            if self._slots is None:  # the shape and kernel are fixed: ask once
+                code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
+                with torch.cuda.device(self.device):
+                    self._slots = _k.splitkv_partial_slots(self.Hq, self.Hkv, self.d, self.block_len,
+                                                           self.max_q_len, code, self.kernel)
+            slots, per_item = self._slots
+            if self.tail_slots is not None:
+                slots = int(self.tail_slots)
+            work, self.n_items, self.part_rows = _k.splitkv_build_work_tail(
+                self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
+                self.n_shards, per_item, slots, self.tail_pieces)
+        elif self.item_blocks > 0:
             work, self.n_items, self.part_rows = _k.splitkv_build_work_split(
                 self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
                 self.n_shards, self.item_blocks)
@@ -89,15 +110,18 @@ class SplitKVAttention:
         if slot[0] is None or slot[0].numel() < work.size:
             slot[0] = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
-        if self._work_dev is None or self._work_dev.numel() < work.size:
-            if self._last_use is not None:
-                self._last_use.synchronize()  # the old buffer is no longer read when it is freed
-            self._work_dev = torch.empty(work.size, dtype=torch.int32, device=self.device)
-        elif self._last_use is not None:
-            st.wait_event(self._last_use)  # the previous batch's calls have read the descriptor
+        b = 1 - self._cur
+        buf = self._work_dev[b]
+        if buf is None or buf.numel() < work.size:
+            if self._last_use[b] is not None:
+                self._last_use[b].synchronize()  # the old buffer is no longer read when it is freed
+            buf = self._work_dev[b] = torch.empty(work.size, dtype=torch.int32, device=self.device)
+        elif self._last_use[b] is not None:
+            st.wait_event(self._last_use[b])  # the calls of two batches back have read this buffer
         slot[0][: work.size].copy_(torch.from_numpy(work))
         with torch.cuda.stream(st):
-            self._work_dev[: work.size].copy_(slot[0][: work.size], non_blocking=True)
+            buf[: work.size].copy_(slot[0][: work.size], non_blocking=True)
+        self._cur = b
         slot[1] = torch.cuda.Event()
         slot[1].record(st)
         self._upload = (slot[1], st)
@@ -124,7 +148,7 @@ class SplitKVAttention:
 
     @property
     def work_device(self):
-        return self._work_dev
+        return self._work_dev[self._cur]
 
     def kernel_used(self):
         if self.kernel != _k.KERNEL_AUTO:
@@ -148,19 +172,20 @@ class SplitKVAttention:
         return st
 
     def _end(self, st):
-        self._last_use = torch.cuda.Event()
-        self._last_use.record(st)
+        ev = torch.cuda.Event()
+        ev.record(st)
+        self._last_use[self._cur] = ev
 
     def partial(self, q, k_pool, v_pool, block_table, scale, stream=None):
         st = self._begin(stream)
-        _k.splitkv_attn_partial(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+        _k.splitkv_attn_partial(q, k_pool, v_pool, block_table, self.work_device, self.n_items, self.B,
                                 self.total_q, self.max_q_len, self.block_len, scale, self.causal,
                                 self._o_part, self._lse_part, kernel=self.kernel, stream=st)
         self._end(st)
 
     def merge(self, out, lse, stream=None):
         st = self._begin(stream)
-        _k.splitkv_merge(self._o_part, self._lse_part, self._work_dev, self.B, self.total_q, out, lse,
+        _k.splitkv_merge(self._o_part, self._lse_part, self.work_device, self.B, self.total_q, out, lse,
                          stream=st)
         self._end(st)
 
@@ -184,11 +209,11 @@ class SplitKVAttention:
             self._grad_pools = (key, torch.zeros(tuple(k_pool.shape), dtype=torch.float32, device=dev),
                                 torch.zeros(tuple(v_pool.shape), dtype=torch.float32, device=dev))
         dk, dv = self._grad_pools[1], self._grad_pools[2]
-        _k.splitkv_attn_backward(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+        _k.splitkv_attn_backward(q, k_pool, v_pool, block_table, self.work_device, self.n_items, self.B,
                                  self.total_q, self.max_q_len, self.block_len, scale, self.causal, dout, lse,
                                  delta, dq_part, dk, dv, stream=stream)
         dq = torch.empty((self.total_q, self.Hq, self.d), dtype=torch.float32, device=dev)
-        _k.splitkv_dq_reduce(dq_part, self._work_dev, self.B, self.total_q, dq, stream=stream)
+        _k.splitkv_dq_reduce(dq_part, self.work_device, self.B, self.total_q, dq, stream=stream)
         self._end(stream)
         return dq, dk, dv
 
@@ -198,7 +223,7 @@ class SplitKVAttention:
             n = _k.splitkv_ticket_count(self.B, self.Hq, self.Hkv, self.max_q_len)
             with torch.cuda.stream(st):
                 self._tickets = torch.zeros(n, dtype=torch.int32, device=self.device)
-        _k.splitkv_attn_fused(q, k_pool, v_pool, block_table, self._work_dev, self.n_items, self.B,
+        _k.splitkv_attn_fused(q, k_pool, v_pool, block_table, self.work_device, self.n_items, self.B,
                               self.total_q, self.max_q_len, self.block_len, scale, self.causal, self._o_part,
                               self._lse_part, self._tickets, out, lse, kernel=self.kernel, stream=st)
         self._end(st)

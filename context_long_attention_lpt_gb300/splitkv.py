@@ -33,6 +33,9 @@ _SIGNATURES = {
     "splitkv_work_words": (_i64, [_i64, _i32]),
     "splitkv_build_work": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _p, _i64, _p, _p]),
     "splitkv_build_work_split": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _p, _i64, _p, _p]),
+    "splitkv_build_work_tail": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _i32, _i32, _p, _i64,
+                                               _p, _p]),
+    "splitkv_partial_slots": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "splitkv_backward_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32]),
     "splitkv_attn_partial": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i32, _p, _i32, _i32, _i32, _i32,
@@ -185,6 +188,32 @@ def splitkv_build_work_split(q_len, kv_len, block_len, block_cost, shard_of_bloc
                                           n_shards, int(max_item_blocks), _ptr(work), words,
                                           ctypes.byref(n_items), ctypes.byref(part_rows)))
     return work, n_items.value, part_rows.value
+
+
+def splitkv_build_work_tail(q_len, kv_len, block_len, block_cost, shard_of_block, n_shards, units_per_item, slots,
+                            pieces):
+    """Returns (work int32 array, n_items, part_rows); the items of the last partial wave
+    (units_per_item CTAs per item, `slots` resident CTAs) cut into up to `pieces` items."""
+    q, kv = _np(q_len, np.int32), _np(kv_len, np.int32)
+    c, sob = _np(block_cost, np.int64), _np(shard_of_block, np.int32)
+    words = splitkv_work_words(len(c), len(q))
+    work = np.zeros(words, dtype=np.int32)
+    n_items = ctypes.c_int32(0)
+    part_rows = ctypes.c_int64(0)
+    _check("splitkv_build_work_tail",
+           lib().splitkv_build_work_tail(_ptr(q), _ptr(kv), len(q), block_len, _ptr(c), _ptr(sob), len(c),
+                                         n_shards, int(units_per_item), int(slots), int(pieces), _ptr(work), words,
+                                         ctypes.byref(n_items), ctypes.byref(part_rows)))
+    return work, n_items.value, part_rows.value
+
+
+def splitkv_partial_slots(Hq, Hkv, d, block_len, max_q_len, dtype, kernel=KERNEL_AUTO):
+    """(CTAs one partial launch keeps resident on the current device, CTAs it launches per
+    work item) for the decode and tensor-core kernels."""
+    per_item = ctypes.c_int32(0)
+    slots = _check("splitkv_partial_slots", lib().splitkv_partial_slots(Hq, Hkv, d, block_len, max_q_len, dtype,
+                                                                        kernel, ctypes.byref(per_item)))
+    return slots, per_item.value
 
 
 def splitkv_auto_kernel(Hq, Hkv, d, block_len, max_q_len, dtype):

@@ -149,6 +149,31 @@ int splitkv_build_work_split(const int32_t* q_len, const int32_t* kv_len, int32_
                              int32_t max_item_blocks, int32_t* work, int64_t work_words,
                              int32_t* n_items, int64_t* part_rows);
 
+/* splitkv_build_work with the items of the last, partly filled wave of CTAs cut
+ * into pieces.  Each item launches units_per_item CTAs, and `slots` CTAs run at
+ * once (both from splitkv_partial_slots).  If the item count times
+ * units_per_item is above `slots` and not a multiple of it, the last
+ * ceil((units mod slots) / units_per_item) items in launch order are each cut
+ * into min(pieces, blocks) items of consecutive blocks, launched last.  The
+ * plan is unchanged (every piece belongs to its shard; the merge reduces the
+ * extra partial rows exactly, Split-KV card, "All Facts"); the last wave's
+ * work is spread over all resident CTAs instead of a few.  units_per_item,
+ * slots or pieces of 0 (or pieces 1): no cut.  Same buffers and statuses as
+ * splitkv_build_work. */
+int splitkv_build_work_tail(const int32_t* q_len, const int32_t* kv_len, int32_t B,
+                            int32_t block_len, const int64_t* block_cost,
+                            const int32_t* shard_of_block, int64_t n_blocks, int32_t n_shards,
+                            int32_t units_per_item, int32_t slots, int32_t pieces, int32_t* work,
+                            int64_t work_words, int32_t* n_items, int64_t* part_rows);
+
+/* CTAs the partial kernel for a shape keeps resident on the current device at
+ * once (occupancy x SM count), returned, and *units_per_item (out) = CTAs it
+ * launches per work item.  kernel: SPLITKV_KERNEL_* (AUTO picks as the
+ * partial call does).  Decode and tensor-core kernels only; other kernels
+ * give SPLITKV_ERR_UNSUPPORTED.  Needs a CUDA device; negative status on error. */
+int splitkv_partial_slots(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len, int32_t max_q_len,
+                          int32_t dtype, int32_t kernel, int32_t* units_per_item);
+
 /* Which kernel SPLITKV_KERNEL_AUTO picks for a shape (a SPLITKV_KERNEL_* value). */
 int splitkv_auto_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32_t block_len,
                         int32_t max_q_len, int32_t dtype);

@@ -239,6 +239,30 @@ def test_runner_on_a_side_stream():
     assert K.splitkv_device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("name", ["decode_small", "shortq_small"])
+def test_next_plan_uploads_while_the_previous_batch_runs(name):
+    """Each plan goes to a copy stream into the descriptor buffer the running batch does not
+    read; plans alternate between two different cuts (different item counts and partial
+    rows), so a batch that read the other buffer, or a buffer still being written, fails."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, device="cuda")
+    up = torch.cuda.Stream()
+    o_ref, l_ref = full_reference(inp)
+    results = []
+    for i in range(8):
+        run.item_blocks = 1 if i % 2 else 0
+        run.plan(stream=up)
+        results.append((run.n_items,) + run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale))
+    torch.cuda.synchronize()
+    assert len({r[0] for r in results}) == 2
+    for n_items, out, lse in results:
+        eo, el = max_errors(out, lse, o_ref, l_ref)
+        assert_close(w, eo, el, f"{name}, plan of {n_items} items uploaded on a copy stream")
+    assert K.splitkv_device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("name", ["shortq_small", "varlen_small", "largest_small", "causal_empty_units"])
 def test_fused_tensor_core_equals_two_launches_bit_for_bit(name):
     """The tensor-core kernel's in-launch merge computes every row as the merge kernel does."""
@@ -310,4 +334,47 @@ def test_split_items_decode_full_size():
         torch.cuda.synchronize()
         eo, el = compare_rows(inp, out, lse, sample_rows(inp, 64, seed=5))
         assert_close(w, eo, el, f"decode, items of 2 blocks, fused={fused}")
+    assert K.splitkv_device_status() == 0
+
+
+@pytest.mark.parametrize("name,slots", [("decode_small", 7), ("shortq_small", 57), ("varlen_small", 11),
+                                        ("specdec_small", 9)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_tail_cut_merges_to_the_unsharded_result(name, slots, fused):
+    """The last partial wave's items cut into pieces (a small resident-CTA count stands in for
+    the device's, so that the small cases have a tail) give the oracle's unsharded attention."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda", poison_tail=True)
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, fused=fused, tail_pieces=3, tail_slots=slots)
+    whole = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                             inp.q.dtype)
+    assert run.n_items > whole.n_items
+    o_ref, l_ref = full_reference(inp)
+    for _ in range(2):
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        torch.cuda.synchronize()
+        eo, el = max_errors(out, lse, o_ref, l_ref)
+        assert_close(w, eo, el, f"{name} tail cut over {slots} slots, fused={fused}")
+    if fused and run.fuses_in_one_launch():
+        assert int(run.tickets.abs().sum()) == 0
+    assert K.splitkv_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["decode", "specdec"])
+def test_tail_cut_full_size_on_the_device_slot_count(name):
+    """Full size, with the resident-CTA count of the device: decode launches 1024 units, which
+    leaves a partial last wave on any GB300 occupancy of 1 or 2 CTAs per SM."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device="cuda")
+    code = K.SPLITKV_BF16
+    slots, per_item = K.splitkv_partial_slots(w.Hq, w.Hkv, w.d, w.block_len, max(inp.q_len), code)
+    assert slots > 0 and per_item >= w.Hkv
+    for fused in (False, True):
+        run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                               inp.q.dtype, fused=fused, tail_pieces=4)
+        out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+        torch.cuda.synchronize()
+        eo, el = compare_rows(inp, out, lse, sample_rows(inp, 64, seed=7))
+        assert_close(w, eo, el, f"{name}, tail cut, fused={fused}")
     assert K.splitkv_device_status() == 0

@@ -300,3 +300,76 @@ def test_fused_launch_count_by_kernel(k):
     assert k.splitkv_fused_launches(32, 8, 128, 1024, 512, 64, BF, k.KERNEL_SIMT) == 2
     with pytest.raises(k.SplitKVError):
         k.splitkv_fused_launches(30, 8, 128, 1024, 512, 64, BF)
+
+
+def _tail_expected(k, q, kv, w, costs, sob, upi, slots, pieces):
+    """The tail cut written out from the plain work lists: the last ceil((units mod slots) /
+    upi) items in launch order, each cut into min(pieces, blocks) runs of consecutive blocks."""
+    plain = _decode_work(k.splitkv_build_work(q, kv, w.block_len, costs, sob, w.n_shards)[0])
+    runs = []
+    for it in plain["items"]:
+        shard, seq, off, cnt = it[:4].tolist()
+        runs.append((shard, seq, plain["blocks"][off: off + cnt].tolist()))
+    n0 = len(runs)
+    units = n0 * upi
+    if upi <= 0 or slots <= 0 or pieces <= 1 or units <= slots or units % slots == 0:
+        return runs
+    tail = -(-(units % slots) // upi)
+    out = runs[: n0 - tail]
+    for shard, seq, blks in runs[n0 - tail:]:
+        p = min(pieces, len(blks))
+        at = 0
+        for j in range(p):
+            c = len(blks) // p + (1 if j < len(blks) % p else 0)
+            out.append((shard, seq, blks[at: at + c]))
+            at += c
+    return out
+
+
+@pytest.mark.parametrize("name,upi,slots,pieces", [("decode", 8, 304, 4), ("decode", 8, 304, 3), ("decode", 8, 1000, 4),
+                                                   ("decode", 8, 256, 4), ("decode", 8, 2048, 4), ("varlen", 40, 152, 4),
+                                                   ("shortq", 64, 152, 8), ("specdec", 8, 152, 2), ("tiny", 4, 3, 4),
+                                                   ("decode", 8, 304, 1), ("decode", 8, 304, 100)])
+def test_tail_work_lists(k, name, upi, slots, pieces):
+    """splitkv_build_work_tail: the items of the last partial wave are cut into runs of
+    consecutive blocks and launched last, the rest is the plain descriptor; every (shard,
+    sequence) pair still holds exactly the plan's key set and the partial rows stay contiguous."""
+    w = wl.WORKLOADS[name]
+    q, kv = wl.lengths(w)
+    costs = k.splitkv_block_costs(q, kv, w.block_len, w.causal)
+    sob, _ = k.splitkv_plan(costs, w.n_shards)
+    work, n_items, part_rows = k.splitkv_build_work_tail(q, kv, w.block_len, costs, sob, w.n_shards, upi, slots,
+                                                         pieces)
+    d = _decode_work(work)
+    want = _tail_expected(k, q, kv, w, costs, sob, upi, slots, pieces)
+    assert n_items == d["n_items"] == len(want)
+    rows = 0
+    gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
+    got = {}
+    for it, (shard, seq, blks) in zip(d["items"], want):
+        s_, b_, off, cnt, prow, clo, chi, _ = it.tolist()
+        assert (s_, b_) == (shard, seq) and d["blocks"][off: off + cnt].tolist() == blks
+        assert prow == rows
+        rows += q[seq]
+        assert ((clo & 0xFFFFFFFF) | (chi << 32)) == sum(costs[gbase[seq] + j] for j in blks)
+        got.setdefault((shard, seq), []).extend(blks)
+    assert rows == part_rows
+    sets = oracle.shard_key_sets(sob.tolist(), kv, w.block_len, w.n_shards)
+    for (shard, seq), blks in got.items():
+        assert sorted(blks) == sets[shard][seq]
+    assert sum(len(v) for s in sets for v in s) == sum(len(v) for v in got.values())
+    for b in range(len(q)):
+        p0, p1 = d["seqs"][b, 3], d["seqs"][b + 1, 3]
+        its = d["seq_items"][p0:p1].tolist()
+        assert sorted(its) == sorted(i for i in range(n_items) if d["items"][i, 1] == b)
+        assert [d["items"][i, 0] for i in its] == sorted(d["items"][i, 0] for i in its)
+
+
+def test_tail_cut_rejects_negative_arguments(k):
+    w = wl.WORKLOADS["decode"]
+    q, kv = wl.lengths(w)
+    costs = k.splitkv_block_costs(q, kv, w.block_len, w.causal)
+    sob, _ = k.splitkv_plan(costs, w.n_shards)
+    for bad in ((-1, 304, 4), (8, -1, 4), (8, 304, -2)):
+        with pytest.raises(k.SplitKVError):
+            k.splitkv_build_work_tail(q, kv, w.block_len, costs, sob, w.n_shards, *bad)
