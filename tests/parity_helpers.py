@@ -47,6 +47,10 @@ SMALL = {
     # one 64-row tile per sequence and ~12 key tiles per dK/dV CTA: K and V are reloaded
     # after every row tile
     "specdec_small": wl.custom("specdec", B=3, context=3000, n_shards=5),
+    # group sizes other than 4 on the tensor-core path: 16 query heads per K/V head
+    # (8 tokens per 128-row tile) and 2
+    "gqa16_tc": wl.custom("shortq", Hq=64, Hkv=4, q_len=20, context=1500, block_len=128, n_shards=3),
+    "gqa2_tc": wl.custom("shortq", Hq=16, Hkv=8, q_len=90, context=1100, block_len=256, n_shards=4),
     "many_key_tiles": wl.custom("shortq", q_len=16, context=24000, block_len=128, n_shards=1),
 }
 

@@ -45,7 +45,8 @@ def _check_every_element(w, inp, out, lse, dout, dq, dk, dv, what):
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_small", "shortq_small", "varlen_small", "noncausal_multi_q",
-                                  "bf16_d64", "largest_small", "causal_empty_units", "many_key_tiles"])
+                                  "bf16_d64", "largest_small", "causal_empty_units", "many_key_tiles",
+                                  "gqa16_tc", "gqa2_tc"])
 def test_backward_matches_oracle(name):
     w = SMALL[name]
     inp, run, out, lse = run_cuda(w)
