@@ -21,8 +21,10 @@
 //    dV += P^T dO and dK += dS^T Q accumulate over all query rows of the
 //    sequence, 64 at a time (two row tiles' S^T | dP^T pairs fit in TMEM, so
 //    the next tile's MMAs run during the key threads' pass).
-// Every wait has a time limit; on expiry the status word gets bit 2 and the
-// CTA unwinds (all MMAs drained, TMEM freed).
+// The MMA warps wait only on named barriers, which the other warps hand over;
+// every mbarrier wait has a time limit.  On expiry the status word gets bit 2,
+// the warp stops waiting and touching TMEM but keeps taking part in every
+// named-barrier hand-off, and the CTA unwinds (all MMAs drained, TMEM freed).
 
 #include <cmath>
 
