@@ -536,6 +536,7 @@ def run_e2e(args, w, inp, run, dev, acc, bound):
     def one():
         for k, v in host.items():
             dbuf[k].copy_(v, non_blocking=True)
+        run.plan()  # block costs, LPT, work lists and their upload, as every step
         out, lse = run(dbuf["q"], dbuf["k_pool"], dbuf["v_pool"], dbuf["block_table"], w.scale)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)

@@ -27,7 +27,9 @@
 //   softmax_X            rows read S_X with tcgen05.ld, keep a running max and
 //                        sum in base 2, and write P_X = exp2(s*c - m) as bf16
 //                        into the first 64 columns of S_X (tcgen05.st);
-//   O_X += P_X V_j       tcgen05.mma with A = P_X from TMEM, B = V_j (MN-major).
+//   O_X += P_X V_j       tcgen05.mma with A = P_X from TMEM, B = V_j (MN-major);
+//                        P_X goes to the MMA warp in two 64-key halves, so the
+//                        first half's PV runs while the second is computed.
 // The tensor pipe runs S_A, S_B, PV_A, S_A', PV_B, S_B', ...: while one query
 // tile's softmax runs, the other tile's MMAs keep the tensor cores busy.  The
 // running max is only moved (and O rescaled through TMEM) when it grows by
@@ -70,6 +72,9 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9, kSyncWarp = 10;
 // warp);  P_B(t) written (the four softmax warps of B).
 constexpr int kBarPrologue = 1, kBarTileA = 2, kBarTileB = 3;
 constexpr int kBarMerge = 4;  // the softmax warps, around the in-launch merge's ticket
+// Second halves of P: keys 64-127 of tile A / B written (the four softmax warps
+// of the tile and the MMA warp)
+constexpr int kBarTileA2 = 5, kBarTileB2 = 6, kBarHalfThreads = 160;
 constexpr int kBarPrologueThreads = 64, kBarTileAThreads = 192, kBarTileBThreads = 160;
 constexpr uint32_t kHalfBytes = kN * 64 * 2;     // 128 rows x 64 bf16 (one swizzled half)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB: one Q, K or V tile
@@ -336,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One elected lane issues every tcgen05.mma and commit (elect.sync keeps
     // the operands on the uniform datapath: an MMA then costs the issuing
     // thread about 17 clk against 48 under a lane test, next to the 64 clk the
-    // tensor pipe takes to run it).  The loop does nothing else per tile: two named-barrier waits (cheap once the
-    // hand-off is there), one shared-memory word, the A and B bursts written
-    // out with their tile index fixed, two commits.  Partial tiles need no
+    // tensor pipe takes to run it).  The loop does nothing else per tile: four named-barrier waits (cheap once
+    // the hand-off is there; one per half of each P), one shared-memory word, the
+    // PV halves and the next S of tiles A and B written out with their tile index
+    // fixed, two commits.  Partial tiles need no
     // branch here (the sync warp zeroed their tail of V); the roles whose waits
     // ran out keep taking part in the hand-offs, so no abort test either.
     const uint32_t idesc_qk = tc::idesc_bf16_f32(kMT, kN, false, false);
@@ -359,11 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::commit(&bar->s_full[x]);
     };
-    // O_X (+)= P_X V(t), P_X from TMEM, V in stage t % kStages; tile 0 starts the sum
-    auto issue_pv = [&](const int x, const int32_t t) {
+    // O_X (+)= P_X V(t) over keys 16 k0 .. 16 k1 - 1, P_X from TMEM, V in stage
+    // t % kStages; tile 0 starts the sum
+    auto issue_pv = [&](const int x, const int32_t t, const int k0, const int k1) {
       const uint32_t o_col = tmem + col_o(x), p_col = tmem + col_s(x), voff = (t % kStages) * kTile16;
 #pragma unroll
-      for (int kk = 0; kk < kN / 16; ++kk)
+      for (int kk = k0; kk < k1; ++kk)
         tc::mma_ts_fast(o_col, p_col + 8 * kk, desc_v0, voff + kk * (2048 >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
     };
     ptx::bar_sync(kBarPrologue, kBarPrologueThreads);  // Q, K(0); bar->first
@@ -375,14 +382,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       for (int32_t t = 0;; ++t) {
-        ptx::bar_sync(kBarTileA, kBarTileAThreads);  // P_A(t); V(t), K(t+1) landed; bar->next
+        ptx::bar_sync(kBarTileA, kBarTileAThreads);  // P_A(t) keys 0-63; V(t), K(t+1) landed; bar->next
         const bool more = *reinterpret_cast<volatile int32_t*>(&bar->next[t & 1]) != 0;
+        tc::fence_after_sync();
+        if (tc::elect_one()) issue_pv(0, t, 0, 4);
+        __syncwarp();
+        ptx::bar_sync(kBarTileA2, kBarHalfThreads);  // P_A(t) keys 64-127
         tc::fence_after_sync();
         if (tc::elect_one()) {
           // While tiles follow, the next S_X commit also covers this PV_X (a
           // commit tracks every earlier MMA of this thread); only the last PV
           // needs its own signal, for the epilogue.
-          issue_pv(0, t);
+          issue_pv(0, t, 4, 8);
           if (more)
             issue_s(0, t + 1);
           else
@@ -390,10 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (has_b) {
-          ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t)
+          ptx::bar_sync(kBarTileB, kBarTileBThreads);  // P_B(t) keys 0-63
+          tc::fence_after_sync();
+          if (tc::elect_one()) issue_pv(1, t, 0, 4);
+          __syncwarp();
+          ptx::bar_sync(kBarTileB2, kBarHalfThreads);  // P_B(t) keys 64-127
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            issue_pv(1, t);
+            issue_pv(1, t, 4, 8);
             if (more)
               issue_s(1, t + 1);
             else
@@ -444,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a wait ran out: no more TMEM work, but every hand-off still takes
           // place (bar.sync keeps this warp in step with the MMA warp)
           ptx::bar_sync(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
+          ptx::bar_sync(x ? kBarTileB2 : kBarTileA2, kBarHalfThreads);
           continue;
         }
         if (release_kv && lane == 0) ptx::mbar_arrive(&bar->kv_free[t % kStages]);  // release t
@@ -506,27 +522,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 sum4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) sum4[k] = make_float2(0.f, 0.f);
-        uint32_t pw[2][32];
+        // P in two halves (keys 0-63 over S columns 0-31, keys 64-127 over 32-63, all
+        // already in registers), each handed to the MMA warp once written, so the
+        // first half's PV runs while the second half is computed.  P_t overwrites
+        // P_{t-1}, which PV_{t-1} read: done, as it was issued before S_t, which
+        // has completed.
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pw[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 xx = ptx::ffma2(make_float2(__uint_as_float(sr[q4][2 * i]), __uint_as_float(sr[q4][2 * i + 1])),
-                                         c2, nmc2);
-            const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-            sum4[i & 3] = add2(sum4[i & 3], pp);
-            pw[q4 >> 1][16 * (q4 & 1) + i] = pack_bf16(pp.x, pp.y);
-          }
+          for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int q4 = 2 * h + qq;
+              const float2 xx = ptx::ffma2(make_float2(__uint_as_float(sr[q4][2 * i]), __uint_as_float(sr[q4][2 * i + 1])),
+                                           c2, nmc2);
+              const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+              sum4[i & 3] = add2(sum4[i & 3], pp);
+              pw[16 * qq + i] = pack_bf16(pp.x, pp.y);
+            }
+          tc::tmem_st32(s_addr + 32 * h, pw);
+          tc::tmem_st_wait();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (h == 0)
+            ptx::bar_arrive(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
+          else
+            ptx::bar_arrive(x ? kBarTileB2 : kBarTileA2, kBarHalfThreads);
+        }
         const float2 s4 = add2(add2(sum4[0], sum4[1]), add2(sum4[2], sum4[3]));
         l += s4.x + s4.y;
-        tc::tmem_st32(s_addr, pw[0]);
-        tc::tmem_st32(s_addr + 32, pw[1]);
-        tc::tmem_st_wait();
-        tc::fence_before_sync();
-        // P_t overwrites P_{t-1}, which PV_{t-1} read: done, as it was issued
-        // before S_t, which has completed.
-        __syncwarp();
-        ptx::bar_arrive(x ? kBarTileB : kBarTileA, x ? kBarTileBThreads : kBarTileAThreads);
       }
     }
     // epilogue: O / l and the log-sum-exp of this row; o_done_x is committed
