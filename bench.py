@@ -328,6 +328,7 @@ def measure_forward(args, dctx, name, dev, headline=False):
     run.plan(stream=upload_stream)
 
     def step(ev=None):
+        run.wait_plan(stream)  # the upload's cross-stream wait stays out of the kernel's events
         if ev is not None:
             ev[0].record(stream)
         if run.fused:

@@ -163,6 +163,12 @@ class SplitKVAttention:
                                          code, self.kernel) == 1
 
     # device steps -----------------------------------------------------------
+    def wait_plan(self, stream=None):
+        """Makes ``stream`` (default: the current stream) wait for the last descriptor upload;
+        the device calls do this themselves when needed, so this only moves the wait earlier
+        (e.g. ahead of an event that should time the kernel alone)."""
+        return self._begin(stream)
+
     def _begin(self, stream):
         """The stream of a device call, made to wait for the work upload if that ran elsewhere."""
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
