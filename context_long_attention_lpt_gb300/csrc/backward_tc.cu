@@ -26,6 +26,7 @@
 // the warp stops waiting and touching TMEM but keeps taking part in every
 // named-barrier hand-off, and the CTA unwinds (all MMAs drained, TMEM freed).
 
+#include <algorithm>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -519,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ========================================================== dK / dV kernel
 
-constexpr int kKeySplit = 16;   // CTAs per (item, K/V head); each takes every 16th key tile
 // Warps 0-7: key threads, two per TMEM lane quarter (warp w: keys of quarter w % 4,
 // rows w / 4 * 32 .. + 31 of each 64-row tile); 8: TMA; 9: MMA; 10: sync warp,
 // which takes the copy waits off the MMA warp.
@@ -600,7 +600,7 @@ __device__ __forceinline__ void key_pass(const uint32_t (&sr)[32], const uint32_
 }
 
 __global__ void __launch_bounds__(kKvThreads, 1)
-    bwd_dkdv_tc_kernel(PartialArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
+    bwd_dkdv_tc_kernel(PartialArgs a, int32_t key_split, const float* __restrict__ lse, const float* __restrict__ delta,
                        float* __restrict__ dk_pool, float* __restrict__ dv_pool,
                        const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
                        const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
@@ -614,9 +614,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   KvBarriers* bar = reinterpret_cast<KvBarriers*>(sdo + kQdStages * kTile64 + kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t split = static_cast<int32_t>(blockIdx.x % kKeySplit);
-  const int32_t kvh = static_cast<int32_t>((blockIdx.x / kKeySplit) % a.Hkv);
-  const int32_t item = static_cast<int32_t>(blockIdx.x / (kKeySplit * a.Hkv));
+  // key_split CTAs per (item, K/V head); CTA `split` takes key tiles split,
+  // split + key_split, ... of the item
+  const int32_t split = static_cast<int32_t>(blockIdx.x % key_split);
+  const int32_t kvh = static_cast<int32_t>((blockIdx.x / key_split) % a.Hkv);
+  const int32_t item = static_cast<int32_t>(blockIdx.x / (static_cast<int64_t>(key_split) * a.Hkv));
 
   const WorkView wv(a.work);
   const int32_t* it = wv.item(item);
@@ -631,10 +633,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tiles.ib = ItemBlocks{wv.blocks() + __ldg(it + kItBlockOff),
                         a.block_table + static_cast<int64_t>(seq) * a.max_blocks_per_seq, __ldg(it + kItBlockCnt),
                         a.block_len, a.max_blocks_per_seq, kv_len, kv_len, a.n_pool_blocks};
-  // this CTA's key tiles: ordinals split, split + kKeySplit, ... of the item's tiles
+  // this CTA's key tiles: ordinals split, split + key_split, ... of the item's tiles
   auto next_mine = [&](TileSeq& w, int32_t& ord, int32_t* pos0, int32_t* nv, int32_t* tok) -> bool {
     while (w.next(pos0, nv, tok)) {
-      if (ord++ % kKeySplit == split) return true;
+      if (ord++ % key_split == split) return true;
     }
     return false;
   };
@@ -997,11 +999,21 @@ int launch_bwd_tc(const PartialArgs& a, const void* dout, const float* lse, cons
                                                                                  tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dQ launch: %s", cudaGetErrorString(e));
-  const int64_t grid_kv = static_cast<int64_t>(kKeySplit) * a.Hkv * a.n_items;
+  // dK/dV CTAs per (item, K/V head): as few as keep about six CTAs per SM in the
+  // launch, so each CTA's set-up, first copies and closing stores cover as many key
+  // tiles as the grid allows (measured: 16 per pair cost 6-8% on the 64-shard
+  // workloads and nearly doubled the decode backward against this choice)
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  const int64_t pairs = static_cast<int64_t>(a.Hkv) * a.n_items;
+  const int32_t key_split = static_cast<int32_t>(std::min<int64_t>(16, std::max<int64_t>(1, (6ll * sms + pairs - 1) / pairs)));
+  const int64_t grid_kv = static_cast<int64_t>(key_split) * pairs;
   if (grid_kv > 0x7fffffffLL) return fail(SPLITKV_ERR_UNSUPPORTED, "too many backward units");
   e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKvSmem));
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward smem attribute: %s", cudaGetErrorString(e));
-  bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kKvThreads, kKvSmem, stream>>>(a, lse, delta, dk_pool, dv_pool,
+  bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid_kv), kKvThreads, kKvSmem, stream>>>(a, key_split, lse, delta, dk_pool, dv_pool,
                                                                                      tq64, tdo64, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPLITKV_ERR_CUDA, "backward dK/dV launch: %s", cudaGetErrorString(e));
