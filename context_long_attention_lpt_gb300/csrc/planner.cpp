@@ -110,7 +110,7 @@ void lpt_order(const int64_t* block_cost, int64_t n_blocks, std::vector<int64_t>
     std::vector<uint64_t> key(static_cast<size_t>(n_blocks));
     for (int64_t g = 0; g < n_blocks; ++g)
       key[g] = ((0xffffffffull - static_cast<uint64_t>(block_cost[g])) << 32) | static_cast<uint64_t>(g);
-    std::sort(key.begin(), key.end());
+    if (!std::is_sorted(key.begin(), key.end())) std::sort(key.begin(), key.end());  // equal costs: sorted
     for (int64_t i = 0; i < n_blocks; ++i) order[i] = static_cast<int64_t>(key[i] & 0xffffffffull);
     return;
   }
@@ -268,13 +268,23 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
       return fail(SPLITKV_ERR_INVALID, "shard_of_block[%lld] = %d out of range", (long long)i,
                   shard_of_block[i]);
 
-  // Group blocks by (shard, sequence); within a group blocks stay ascending.
+  // Group blocks by (shard, sequence); within a group blocks stay ascending.  A
+  // counting sort on shard * B + sequence when there are not many more groups
+  // than blocks, else a stable comparison sort: the same order either way.
   std::vector<int64_t> idx(static_cast<size_t>(n_blocks));
-  for (int64_t i = 0; i < n_blocks; ++i) idx[i] = i;
-  std::stable_sort(idx.begin(), idx.end(), [&](int64_t x, int64_t y) {
-    if (shard_of_block[x] != shard_of_block[y]) return shard_of_block[x] < shard_of_block[y];
-    return seq_of[x] < seq_of[y];
-  });
+  const int64_t groups = static_cast<int64_t>(n_shards) * B;
+  if (groups <= 4 * n_blocks + 4096) {
+    std::vector<int64_t> start(static_cast<size_t>(groups) + 1, 0);
+    for (int64_t i = 0; i < n_blocks; ++i) ++start[static_cast<int64_t>(shard_of_block[i]) * B + seq_of[i] + 1];
+    for (int64_t k = 0; k < groups; ++k) start[k + 1] += start[k];
+    for (int64_t i = 0; i < n_blocks; ++i) idx[start[static_cast<int64_t>(shard_of_block[i]) * B + seq_of[i]]++] = i;
+  } else {
+    for (int64_t i = 0; i < n_blocks; ++i) idx[i] = i;
+    std::stable_sort(idx.begin(), idx.end(), [&](int64_t x, int64_t y) {
+      if (shard_of_block[x] != shard_of_block[y]) return shard_of_block[x] < shard_of_block[y];
+      return seq_of[x] < seq_of[y];
+    });
+  }
   struct Item {
     int32_t shard, seq;
     int64_t first, count, cost;

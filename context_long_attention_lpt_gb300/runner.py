@@ -6,6 +6,8 @@
     copy work descriptor to the device
     splitkv_attn_partial -> splitkv_merge                        (device, one stream)
 
+(the first two lines are one call, splitkv_plan_batch, for the plain LPT plan).
+
 It owns the device buffers the calls need (work descriptor, partials, outputs),
 allocated with torch and reused across calls of the same shape.  It computes
 nothing itself.
@@ -60,6 +62,11 @@ class SplitKVAttention:
         # (a few KB each; eight steps absorb a host stall of about a millisecond on
         # the shortest workloads)
         self._ring = [[None, None] for _ in range(8)]  # [pinned buffer, upload-done event]
+        n_blocks = _k.splitkv_num_blocks(self._kv_len_np, self.block_len)
+        self._words = _k.splitkv_work_words(n_blocks, self.B)
+        self.block_cost = np.zeros(n_blocks, dtype=np.int64)  # outputs of the one-call plan
+        self.shard_of_block = np.zeros(n_blocks, dtype=np.int32)
+        self.shard_load = np.zeros(self.n_shards, dtype=np.int64)
         self._ring_next = 0
         self._work_dev = [None, None]  # device descriptors, used in turn
         self._cur = 1                  # the buffer the device calls read (flipped by each plan)
@@ -67,12 +74,55 @@ class SplitKVAttention:
         self._lse_part = None
         self._upload = None            # (event, stream) of the last work upload
         self._last_use = [None, None]  # per buffer: event after the last device call that read it
+        self._use_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self.plan()
 
     # host steps -------------------------------------------------------------
     def plan(self, stream=None):
         """Block costs, LPT plan and work lists on the host; copy the work to the device on
-        ``stream`` (default: the current stream)."""
+        ``stream`` (default: the current stream).  The plain LPT plan takes one library call
+        (splitkv_plan_batch), which also queues the copy; split selection and cut items take the
+        separate calls."""
+        if self.tail_pieces > 1 and self.item_blocks > 0:
+            raise ValueError("tail_pieces and item_blocks are exclusive")
+        one_call = self.planner == "lpt" and self.tail_pieces <= 1 and self.item_blocks <= 0
+        if not one_call:
+            work = self._plan_steps()
+        slot = self._ring[self._ring_next]
+        self._ring_next = (self._ring_next + 1) % len(self._ring)
+        if slot[1] is None:
+            slot[0] = torch.empty(self._words, dtype=torch.int32, pin_memory=True)
+            slot[1] = torch.cuda.Event()
+        else:
+            slot[1].synchronize()  # this buffer's last upload has left it
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        b = 1 - self._cur
+        buf = self._work_dev[b]
+        if buf is None:
+            buf = self._work_dev[b] = torch.empty(self._words, dtype=torch.int32, device=self.device)
+        elif self._last_use[b] is not None:
+            st.wait_event(self._last_use[b])  # the calls of two batches back have read this buffer
+        if one_call:
+            self.n_items, self.part_rows = _k.splitkv_plan_batch(
+                self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.block_cost,
+                self.shard_of_block, self.shard_load, slot[0], buf, st)
+        else:
+            slot[0].copy_(torch.from_numpy(work))
+            with torch.cuda.stream(st):
+                buf.copy_(slot[0], non_blocking=True)
+        self._cur = b
+        slot[1].record(st)
+        self._upload = (slot[1], st)
+        self._host_slot = slot[0]
+        if self._o_part is None or self._o_part.shape[0] < self.part_rows:
+            self._o_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32,
+                                       device=self.device)
+            self._lse_part = torch.empty((max(self.part_rows, 1), self.Hq), dtype=torch.float32,
+                                         device=self.device)
+        return self
+
+    def _plan_steps(self):
+        """The host steps as separate library calls (split selection, cut items)."""
         self.block_cost = _k.splitkv_block_costs(self._q_len_np, self._kv_len_np, self.block_len,
                                                  self.causal)
         if self.planner == "lpt":
@@ -81,8 +131,6 @@ class SplitKVAttention:
             self.n_shards_used, self.shard_of_block, self.shard_load, self.modeled_time = _k.splitkv_plan_dcp(
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
                 self.dcp_beta, self.dcp_gamma)
-        if self.tail_pieces > 1 and self.item_blocks > 0:
-            raise ValueError("tail_pieces and item_blocks are exclusive")
         if self.tail_pieces > 1:
             if self._slots is None:  # the shape and kernel are fixed: ask once
                 code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
@@ -103,35 +151,12 @@ class SplitKVAttention:
             work, self.n_items, self.part_rows = _k.splitkv_build_work(
                 self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
                 self.n_shards)
-        slot = self._ring[self._ring_next]
-        self._ring_next = (self._ring_next + 1) % len(self._ring)
-        if slot[1] is not None:
-            slot[1].synchronize()  # this buffer's last upload has left it
-        if slot[0] is None or slot[0].numel() < work.size:
-            slot[0] = torch.empty(work.size, dtype=torch.int32, pin_memory=True)
-        st = stream if stream is not None else torch.cuda.current_stream(self.device)
-        b = 1 - self._cur
-        buf = self._work_dev[b]
-        if buf is None or buf.numel() < work.size:
-            if self._last_use[b] is not None:
-                self._last_use[b].synchronize()  # the old buffer is no longer read when it is freed
-            buf = self._work_dev[b] = torch.empty(work.size, dtype=torch.int32, device=self.device)
-        elif self._last_use[b] is not None:
-            st.wait_event(self._last_use[b])  # the calls of two batches back have read this buffer
-        slot[0][: work.size].copy_(torch.from_numpy(work))
-        with torch.cuda.stream(st):
-            buf[: work.size].copy_(slot[0][: work.size], non_blocking=True)
-        self._cur = b
-        slot[1] = torch.cuda.Event()
-        slot[1].record(st)
-        self._upload = (slot[1], st)
-        self.work_host = work
-        if self._o_part is None or self._o_part.shape[0] < self.part_rows:
-            self._o_part = torch.empty((max(self.part_rows, 1), self.Hq, self.d), dtype=torch.float32,
-                                       device=self.device)
-            self._lse_part = torch.empty((max(self.part_rows, 1), self.Hq), dtype=torch.float32,
-                                         device=self.device)
-        return self
+        return work
+
+    @property
+    def work_host(self):
+        """A copy of the current plan's work descriptor (int32 numpy)."""
+        return self._host_slot.numpy().copy()
 
     @property
     def imbalance(self):
@@ -178,7 +203,7 @@ class SplitKVAttention:
         return st
 
     def _end(self, st):
-        ev = torch.cuda.Event()
+        ev = self._use_ev[self._cur]  # re-recorded: a later wait sees the last device call
         ev.record(st)
         self._last_use[self._cur] = ev
 

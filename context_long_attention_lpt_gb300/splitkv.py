@@ -35,6 +35,8 @@ _SIGNATURES = {
     "splitkv_build_work_split": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _p, _i64, _p, _p]),
     "splitkv_build_work_tail": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _i32, _i32, _p, _i64,
                                                _p, _p]),
+    "splitkv_plan_batch": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _p, _i64, _p, _p,
+                                          _p]),
     "splitkv_partial_slots": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "splitkv_backward_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32]),
@@ -205,6 +207,45 @@ def splitkv_build_work_tail(q_len, kv_len, block_len, block_cost, shard_of_block
                                          n_shards, int(units_per_item), int(slots), int(pieces), _ptr(work), words,
                                          ctypes.byref(n_items), ctypes.byref(part_rows)))
     return work, n_items.value, part_rows.value
+
+
+def _host_out(a, dtype, name):
+    if not (isinstance(a, np.ndarray) and a.dtype == dtype and a.flags.c_contiguous and a.flags.writeable):
+        raise TypeError(f"{name} must be a writeable contiguous {np.dtype(dtype).name} numpy array")
+    return a.ctypes.data
+
+
+def splitkv_plan_batch(q_len, kv_len, block_len, causal, n_shards, block_cost, shard_of_block, shard_load,
+                       work_host, work_dev=None, stream=None):
+    """Block costs, LPT plan, work lists and the descriptor upload in one library call.
+    q_len, kv_len: [B] sequence lengths; block_cost (int64 [n_blocks]), shard_of_block (int32
+    [n_blocks]) and shard_load (int64 [n_shards]) are numpy outputs; work_host is the int32
+    descriptor output, a CPU tensor (page-locked for an asynchronous copy) or a numpy array;
+    work_dev an int32 device tensor of the same length, or None for no copy.  The copy runs on
+    ``stream`` (default: the current stream).  Returns (n_items, part_rows)."""
+    q_len, kv_len = _np(q_len, np.int32), _np(kv_len, np.int32)
+    if len(q_len) != len(kv_len):
+        raise ValueError("q_len and kv_len must have one entry per sequence")
+    n_blocks = len(block_cost)
+    if len(shard_of_block) != n_blocks or len(shard_load) != n_shards:
+        raise ValueError("shard_of_block must have n_blocks entries and shard_load n_shards")
+    if isinstance(work_host, np.ndarray):
+        wh, words = _host_out(work_host, np.int32, "work_host"), work_host.size
+    else:
+        if work_host.device.type != "cpu" or not work_host.is_contiguous() or work_host.element_size() != 4:
+            raise TypeError("work_host must be a contiguous int32 CPU tensor or numpy array")
+        wh, words = work_host.data_ptr(), work_host.numel()
+    wd, sh = None, None
+    if work_dev is not None:
+        if work_dev.numel() != words or not work_dev.is_contiguous() or work_dev.element_size() != 4:
+            raise ValueError("work_dev must be a contiguous int32 tensor as long as work_host")
+        wd, sh = work_dev.data_ptr(), _stream_handle(stream)
+    n_items, part_rows = ctypes.c_int32(0), ctypes.c_int64(0)
+    _check("splitkv_plan_batch", lib().splitkv_plan_batch(
+        q_len.ctypes.data, kv_len.ctypes.data, len(q_len), block_len, int(bool(causal)), n_shards, _host_out(block_cost, np.int64, "block_cost"),
+        _host_out(shard_of_block, np.int32, "shard_of_block"), n_blocks, _host_out(shard_load, np.int64, "shard_load"),
+        wh, wd, words, ctypes.byref(n_items), ctypes.byref(part_rows), sh))
+    return n_items.value, part_rows.value
 
 
 def splitkv_partial_slots(Hq, Hkv, d, block_len, max_q_len, dtype, kernel=KERNEL_AUTO):

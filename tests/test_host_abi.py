@@ -373,3 +373,48 @@ def test_tail_cut_rejects_negative_arguments(k):
     for bad in ((-1, 304, 4), (8, -1, 4), (8, 304, -2)):
         with pytest.raises(k.SplitKVError):
             k.splitkv_build_work_tail(q, kv, w.block_len, costs, sob, w.n_shards, *bad)
+
+
+def _plan_batch(k, q, kv, bl, causal, S, words=None):
+    n = k.splitkv_num_blocks(kv, bl)
+    cost, sob, load = np.zeros(n, np.int64), np.zeros(n, np.int32), np.zeros(S, np.int64)
+    work = np.zeros(words if words is not None else k.splitkv_work_words(n, len(q)), np.int32)
+    n_items, part_rows = k.splitkv_plan_batch(q, kv, bl, causal, S, cost, sob, load, work)
+    return cost, sob, load, work, n_items, part_rows
+
+
+def test_plan_batch_is_the_three_calls(k):
+    """The one-call plan gives the oracle's costs and LPT plan and the same descriptor as
+    splitkv_build_work, on every workload and on fuzz cases."""
+    rng = random.Random(77)
+    cases = [(*wl.lengths(w), w.block_len, w.causal, w.n_shards) for w in wl.WORKLOADS.values()]
+    for _ in range(300):
+        B = rng.randint(1, 5)
+        q = [rng.randint(0, 40) for _ in range(B)]
+        kv = [qq + rng.randint(0 if qq else 1, 300) for qq in q]
+        cases.append((q, kv, rng.choice([1, 4, 16, 64]), rng.random() < 0.6, rng.randint(1, 9)))
+    for q, kv, bl, causal, S in cases:
+        cost, sob, load, work, n_items, part_rows = _plan_batch(k, q, kv, bl, causal, S)
+        ref_cost = oracle.block_costs(q, kv, bl, causal)
+        ref_sob, ref_load = oracle.lpt_assign(ref_cost, S)
+        assert cost.tolist() == ref_cost and sob.tolist() == ref_sob and load.tolist() == ref_load
+        ref_work, ref_items, ref_rows = k.splitkv_build_work(q, kv, bl, cost, sob, S)
+        assert np.array_equal(work, ref_work) and (n_items, part_rows) == (ref_items, ref_rows)
+
+
+def test_plan_batch_errors(k):
+    w = wl.WORKLOADS["shortq"]
+    q, kv = wl.lengths(w)
+    n = k.splitkv_num_blocks(kv, w.block_len)
+    words = k.splitkv_work_words(n, len(q))
+    with pytest.raises(k.SplitKVError) as e:
+        _plan_batch(k, q, kv, w.block_len, w.causal, w.n_shards, words=words - 1)
+    assert e.value.status == -4
+    cost, sob, load = np.zeros(n + 1, np.int64), np.zeros(n + 1, np.int32), np.zeros(w.n_shards, np.int64)
+    with pytest.raises(k.SplitKVError):  # n_blocks does not match the batch
+        k.splitkv_plan_batch(q, kv, w.block_len, w.causal, w.n_shards, cost, sob, load, np.zeros(words + 8, np.int32))
+    with pytest.raises(TypeError):  # outputs of the wrong type are refused before the call
+        k.splitkv_plan_batch(q, kv, w.block_len, w.causal, w.n_shards, cost[:n].astype(np.int32), sob[:n], load,
+                             np.zeros(words, np.int32))
+    with pytest.raises(k.SplitKVError):
+        k.splitkv_plan_batch(q, kv, w.block_len, w.causal, 0, cost[:n], sob[:n], load[:0], np.zeros(words, np.int32))
