@@ -60,9 +60,10 @@ def parse_args(argv=None):
     ap.add_argument("--planner", choices=["lpt", "dcp"], default="lpt",
                     help="lpt: cost-aware LPT onto all shards; dcp: shard count chosen by the attention + "
                          "reduction completion model (splitkv_plan_dcp)")
-    ap.add_argument("--tail-pieces", type=int, default=0,
+    ap.add_argument("--tail-pieces", type=int, default=None,
                     help="cut the items of the last partial wave of CTAs into this many pieces "
-                         "(splitkv_build_work_tail; 0: no cut)")
+                         "(splitkv_build_work_tail; 0: no cut; default: the runner's choice, 4 on the decode "
+                         "kernel and none elsewhere)")
     ap.add_argument("--item-blocks", type=int, default=0,
                     help="cut work items into runs of at most this many blocks (0: one item per shard and "
                          "sequence)")
@@ -312,7 +313,7 @@ def measure_forward(args, dctx, name, dev, headline=False):
                            inp.q.dtype, device=f"cuda:{dev}", kernel=kernel, fused=args.fused,
                            planner=args.planner, dcp_alpha=alpha, dcp_beta=beta, dcp_gamma=gamma,
                            item_blocks=args.item_blocks if headline else 0,
-                           tail_pieces=args.tail_pieces if headline else 0)
+                           tail_pieces=args.tail_pieces if headline else None)
     fused_one_launch = run.fused and run.fuses_in_one_launch()
     out = torch.empty((run.total_q, w.Hq, w.d), dtype=inp.q.dtype, device=f"cuda:{dev}")
     lse = torch.empty((run.total_q, w.Hq), dtype=torch.float32, device=f"cuda:{dev}")
@@ -386,7 +387,8 @@ def measure_forward(args, dctx, name, dev, headline=False):
     fields = {
         "value": units / t_max / scale, "unit": unit, "ms_per_step": 1e3 * t_max / args.steps,
         "steps": args.steps, "kv_gbs": kv_all / t_max / 1e9, "tflops": fl_all / t_max / 1e12,
-        "shape": w.description, "kernel": kname, "n_items": run.n_items, "lpt_imbalance": run.imbalance,
+        "shape": w.description, "kernel": kname, "n_items": run.n_items, "tail_pieces": run.tail_pieces,
+        "lpt_imbalance": run.imbalance,
         "planner": args.planner, "shards_used": run.n_shards_used, "part_rows": run.part_rows,
         "host_s": host_s, "roofline": roof, "clocks": clocks,
         "gpu_launches": (1 if fused_one_launch else 2) * args.steps,
@@ -495,7 +497,8 @@ def run_ours(args, dctx):
         del objs
         torch.cuda.empty_cache()
         per[name] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "steps", "kv_gbs", "tflops", "shape",
-                                        "kernel", "n_items", "lpt_imbalance", "shards_used", "part_rows",
+                                        "kernel", "n_items", "tail_pieces", "lpt_imbalance", "shards_used",
+                                        "part_rows",
                                         "roofline", "clocks", "gpu_launches", "l2")}
     for name in [x for x in args.per_backward.split(",") if x]:
         per[f"backward/{name}"] = measure_backward(args, dctx, name, dev)
@@ -507,6 +510,7 @@ def run_ours(args, dctx):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "kv_gbs": f["kv_gbs"], "tflops": f["tflops"],
         "config": {"workload": w.name, "shape": f["shape"], "kernel": f["kernel"], "n_items": f["n_items"],
+                   "tail_pieces": f["tail_pieces"],
                    "lpt_imbalance": f["lpt_imbalance"], "planner": f["planner"], "shards_used": f["shards_used"],
                    "part_rows": f["part_rows"], "planner_us": planner_us, "host_s": f["host_s"], "l2": f["l2"],
                    "parallelism": f"replicas x{dctx.world}"},

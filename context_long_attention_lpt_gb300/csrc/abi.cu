@@ -95,15 +95,15 @@ extern "C" int splitkv_backward_kernel(int32_t Hq, int32_t Hkv, int32_t d, int32
 }
 
 extern "C" int splitkv_plan_batch(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
-                                  int32_t causal, int32_t n_shards, int64_t* block_cost, int32_t* shard_of_block,
-                                  int64_t n_blocks, int64_t* shard_load, int32_t* work_host, int32_t* work_dev,
-                                  int64_t work_words, int32_t* n_items, int64_t* part_rows, void* stream) {
+                                  int32_t causal, int32_t n_shards, int32_t units_per_item, int32_t slots,
+                                  int32_t pieces, int64_t* block_cost, int32_t* shard_of_block, int64_t n_blocks,
+                                  int64_t* shard_load, int32_t* work_host, int32_t* work_dev, int64_t work_words, int32_t* n_items, int64_t* part_rows, void* stream) {
   int st = splitkv_block_costs(q_len, kv_len, B, block_len, causal, block_cost, n_blocks);
   if (st != SPLITKV_OK) return st;
   st = splitkv_plan(block_cost, n_blocks, n_shards, shard_of_block, shard_load);
   if (st != SPLITKV_OK) return st;
-  st = splitkv_build_work(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards, work_host,
-                          work_words, n_items, part_rows);
+  st = splitkv_build_work_tail(q_len, kv_len, B, block_len, block_cost, shard_of_block, n_blocks, n_shards,
+                               units_per_item, slots, pieces, work_host, work_words, n_items, part_rows);
   if (st != SPLITKV_OK) return st;
   if (work_dev) {
     const cudaError_t e = cudaMemcpyAsync(work_dev, work_host, static_cast<size_t>(work_words) * sizeof(int32_t),

@@ -30,7 +30,7 @@ from . import splitkv as _k
 class SplitKVAttention:
     def __init__(self, q_len, kv_len, block_len, causal, n_shards, Hq, Hkv, d, dtype,
                  device="cuda", kernel=_k.KERNEL_AUTO, fused=False, planner="lpt", dcp_alpha=1.0,
-                 dcp_beta=0.0, dcp_gamma=0.0, item_blocks=0, tail_pieces=0, tail_slots=None):
+                 dcp_beta=0.0, dcp_gamma=0.0, item_blocks=0, tail_pieces=None, tail_slots=None):
         self.q_len = [int(x) for x in q_len]
         self.kv_len = [int(x) for x in kv_len]
         self.B = len(self.q_len)
@@ -48,13 +48,19 @@ class SplitKVAttention:
         self.dcp_alpha, self.dcp_beta, self.dcp_gamma = float(dcp_alpha), float(dcp_beta), float(dcp_gamma)
         self.n_shards_used = self.n_shards
         self.item_blocks = int(item_blocks)  # > 0: work items of at most this many blocks
-        self.tail_pieces = int(tail_pieces)  # > 1: the last partial wave's items cut into this many
+        self.tail_pieces = tail_pieces  # > 1: the last partial wave's items cut into this many (set below)
         self.tail_slots = tail_slots  # resident CTAs assumed by the cut (None: the library's count)
         self._slots = None
         self._tickets = None
         self._grad_pools = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
+        if self.tail_pieces is None:
+            # Default: cut the last partial wave into 4 pieces on the decode kernel, whose lone
+            # CTAs stream slowly (decode step: 184 -> 176 us); no cut elsewhere (the tensor-core
+            # kernel on 16 query rows: 200 -> 208 us with 4 pieces).
+            self.tail_pieces = 4 if self.item_blocks <= 0 and self.kernel_used() == _k.KERNEL_DECODE else 0
+        self.tail_pieces = int(self.tail_pieces)
         self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
         self._kv_len_np = np.asarray(self.kv_len, dtype=np.int32)
         # pinned staging buffers for the work list, used in turn, so planning the
@@ -80,14 +86,16 @@ class SplitKVAttention:
     # host steps -------------------------------------------------------------
     def plan(self, stream=None):
         """Block costs, LPT plan and work lists on the host; copy the work to the device on
-        ``stream`` (default: the current stream).  The plain LPT plan takes one library call
-        (splitkv_plan_batch), which also queues the copy; split selection and cut items take the
-        separate calls."""
+        ``stream`` (default: the current stream).  The LPT plan, with or without the tail cut,
+        takes one library call (splitkv_plan_batch), which also queues the copy; split selection
+        and items of bounded length take the separate calls."""
         if self.tail_pieces > 1 and self.item_blocks > 0:
             raise ValueError("tail_pieces and item_blocks are exclusive")
-        one_call = self.planner == "lpt" and self.tail_pieces <= 1 and self.item_blocks <= 0
+        one_call = self.planner == "lpt" and self.item_blocks <= 0
         if not one_call:
             work = self._plan_steps()
+        else:
+            upi, slots = self._tail_slots() if self.tail_pieces > 1 else (0, 0)
         slot = self._ring[self._ring_next]
         self._ring_next = (self._ring_next + 1) % len(self._ring)
         if slot[1] is None:
@@ -105,7 +113,7 @@ class SplitKVAttention:
         if one_call:
             self.n_items, self.part_rows = _k.splitkv_plan_batch(
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.block_cost,
-                self.shard_of_block, self.shard_load, slot[0], buf, st)
+                self.shard_of_block, self.shard_load, slot[0], buf, st, upi, slots, self.tail_pieces)
         else:
             slot[0].copy_(torch.from_numpy(work))
             with torch.cuda.stream(st):
@@ -122,7 +130,7 @@ class SplitKVAttention:
         return self
 
     def _plan_steps(self):
-        """The host steps as separate library calls (split selection, cut items)."""
+        """The host steps as separate library calls."""
         self.block_cost = _k.splitkv_block_costs(self._q_len_np, self._kv_len_np, self.block_len,
                                                  self.causal)
         if self.planner == "lpt":
@@ -132,14 +140,7 @@ class SplitKVAttention:
                 self._q_len_np, self._kv_len_np, self.block_len, self.causal, self.n_shards, self.dcp_alpha,
                 self.dcp_beta, self.dcp_gamma)
         if self.tail_pieces > 1:
-            if self._slots is None:  # the shape and kernel are fixed: ask once
-                code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
-                with torch.cuda.device(self.device):
-                    self._slots = _k.splitkv_partial_slots(self.Hq, self.Hkv, self.d, self.block_len,
-                                                           self.max_q_len, code, self.kernel)
-            slots, per_item = self._slots
-            if self.tail_slots is not None:
-                slots = int(self.tail_slots)
+            per_item, slots = self._tail_slots()
             work, self.n_items, self.part_rows = _k.splitkv_build_work_tail(
                 self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
                 self.n_shards, per_item, slots, self.tail_pieces)
@@ -152,6 +153,16 @@ class SplitKVAttention:
                 self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
                 self.n_shards)
         return work
+
+    def _tail_slots(self):
+        """(CTAs per work item, resident CTAs) for the tail cut."""
+        if self._slots is None:  # the shape and kernel are fixed: ask once
+            code = _k.SPLITKV_F32 if self.dtype == torch.float32 else _k.SPLITKV_BF16
+            with torch.cuda.device(self.device):
+                self._slots = _k.splitkv_partial_slots(self.Hq, self.Hkv, self.d, self.block_len,
+                                                       self.max_q_len, code, self.kernel)
+        slots, per_item = self._slots
+        return per_item, (int(self.tail_slots) if self.tail_slots is not None else slots)
 
     @property
     def work_host(self):

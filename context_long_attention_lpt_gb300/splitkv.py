@@ -35,8 +35,8 @@ _SIGNATURES = {
     "splitkv_build_work_split": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _p, _i64, _p, _p]),
     "splitkv_build_work_tail": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _i32, _i32, _i32, _i32, _p, _i64,
                                                _p, _p]),
-    "splitkv_plan_batch": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _p, _i64, _p, _p,
-                                          _p]),
+    "splitkv_plan_batch": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _p,
+                                          _i64, _p, _p, _p]),
     "splitkv_partial_slots": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
     "splitkv_auto_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "splitkv_backward_kernel": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32]),
@@ -216,13 +216,14 @@ def _host_out(a, dtype, name):
 
 
 def splitkv_plan_batch(q_len, kv_len, block_len, causal, n_shards, block_cost, shard_of_block, shard_load,
-                       work_host, work_dev=None, stream=None):
+                       work_host, work_dev=None, stream=None, units_per_item=0, slots=0, pieces=0):
     """Block costs, LPT plan, work lists and the descriptor upload in one library call.
     q_len, kv_len: [B] sequence lengths; block_cost (int64 [n_blocks]), shard_of_block (int32
     [n_blocks]) and shard_load (int64 [n_shards]) are numpy outputs; work_host is the int32
     descriptor output, a CPU tensor (page-locked for an asynchronous copy) or a numpy array;
     work_dev an int32 device tensor of the same length, or None for no copy.  The copy runs on
-    ``stream`` (default: the current stream).  Returns (n_items, part_rows)."""
+    ``stream`` (default: the current stream).  units_per_item, slots, pieces: the tail cut of
+    splitkv_build_work_tail (pieces <= 1: none).  Returns (n_items, part_rows)."""
     q_len, kv_len = _np(q_len, np.int32), _np(kv_len, np.int32)
     if len(q_len) != len(kv_len):
         raise ValueError("q_len and kv_len must have one entry per sequence")
@@ -242,7 +243,8 @@ def splitkv_plan_batch(q_len, kv_len, block_len, causal, n_shards, block_cost, s
         wd, sh = work_dev.data_ptr(), _stream_handle(stream)
     n_items, part_rows = ctypes.c_int32(0), ctypes.c_int64(0)
     _check("splitkv_plan_batch", lib().splitkv_plan_batch(
-        q_len.ctypes.data, kv_len.ctypes.data, len(q_len), block_len, int(bool(causal)), n_shards, _host_out(block_cost, np.int64, "block_cost"),
+        q_len.ctypes.data, kv_len.ctypes.data, len(q_len), block_len, int(bool(causal)), n_shards,
+        int(units_per_item), int(slots), int(pieces), _host_out(block_cost, np.int64, "block_cost"),
         _host_out(shard_of_block, np.int32, "shard_of_block"), n_blocks, _host_out(shard_load, np.int64, "shard_load"),
         wh, wd, words, ctypes.byref(n_items), ctypes.byref(part_rows), sh))
     return n_items.value, part_rows.value

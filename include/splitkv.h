@@ -168,8 +168,9 @@ int splitkv_build_work_tail(const int32_t* q_len, const int32_t* kv_len, int32_t
 
 /* Steps 1-2 and the descriptor upload of one batch in one call: block costs
  * (Split-KV card, "Timeline": cost-aware), the LPT plan and the work lists,
- * exactly as splitkv_block_costs -> splitkv_plan -> splitkv_build_work, then
- * an asynchronous copy of the descriptor's work_words words from work_host to
+ * exactly as splitkv_block_costs -> splitkv_plan -> splitkv_build_work_tail
+ * (units_per_item, slots, pieces as there; pieces <= 1: no cut, the descriptor
+ * of splitkv_build_work), then an asynchronous copy of the descriptor's work_words words from work_host to
  * work_dev on `stream` (a cudaStream_t; NULL is the legacy default stream).
  * For callers that plan every step, where one call instead of three keeps the
  * host ahead of the device.
@@ -185,8 +186,9 @@ int splitkv_build_work_tail(const int32_t* q_len, const int32_t* kv_len, int32_t
  * Statuses: those of the three calls (nothing is copied when one fails),
  * SPLITKV_ERR_CUDA when the copy cannot be queued. */
 int splitkv_plan_batch(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t block_len,
-                       int32_t causal, int32_t n_shards, int64_t* block_cost,
-                       int32_t* shard_of_block, int64_t n_blocks, int64_t* shard_load,
+                       int32_t causal, int32_t n_shards, int32_t units_per_item, int32_t slots,
+                       int32_t pieces, int64_t* block_cost, int32_t* shard_of_block,
+                       int64_t n_blocks, int64_t* shard_load,
                        int32_t* work_host, int32_t* work_dev, int64_t work_words,
                        int32_t* n_items, int64_t* part_rows, void* stream);
 

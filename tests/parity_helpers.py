@@ -55,10 +55,10 @@ SMALL = {
 }
 
 
-def run_cuda(w, kernel=0, poison=True, device="cuda", spare_blocks=0, lens=None):
+def run_cuda(w, kernel=0, poison=True, device="cuda", spare_blocks=0, lens=None, **runner_kw):
     inp = wl.make_inputs(w, device=device, poison_tail=poison, spare_blocks=spare_blocks, lens=lens)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
-                           inp.q.dtype, device=device, kernel=kernel)
+                           inp.q.dtype, device=device, kernel=kernel, **runner_kw)
     out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
     torch.cuda.synchronize()
     return inp, run, out, lse

@@ -54,9 +54,10 @@ def test_tensor_core_few_tile_items(seed):
 @pytest.mark.parametrize("kernel", [K.KERNEL_AUTO, K.KERNEL_SIMT])
 @pytest.mark.parametrize("name", ["decode_small", "shortq_small", "varlen_small", "tiny", "causal_empty_units"])
 def test_partials_match_oracle_partials(name, kernel):
-    """Each work item's (O_i, L_i) equals the oracle's partial over the oracle's own shard."""
+    """Each work item's (O_i, L_i) equals the oracle's partial over the oracle's own shard
+    (items uncut, so each item is a whole (shard, sequence) pair)."""
     w = SMALL[name]
-    inp, run, _, _ = run_cuda(w, kernel=kernel)
+    inp, run, _, _ = run_cuda(w, kernel=kernel, tail_pieces=0)
     costs = oracle.block_costs(inp.q_len, inp.kv_len, w.block_len, w.causal)
     sob, _ = oracle.lpt_assign(costs, w.n_shards)
     sets = oracle.shard_key_sets(sob, inp.kv_len, w.block_len, w.n_shards)
@@ -247,7 +248,7 @@ def test_next_plan_uploads_while_the_previous_batch_runs(name):
     w = SMALL[name]
     inp = wl.make_inputs(w, device="cuda", poison_tail=True)
     run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
-                           inp.q.dtype, device="cuda")
+                           inp.q.dtype, device="cuda", tail_pieces=0)
     up = torch.cuda.Stream()
     o_ref, l_ref = full_reference(inp)
     results = []

@@ -375,17 +375,20 @@ def test_tail_cut_rejects_negative_arguments(k):
             k.splitkv_build_work_tail(q, kv, w.block_len, costs, sob, w.n_shards, *bad)
 
 
-def _plan_batch(k, q, kv, bl, causal, S, words=None):
+def _plan_batch(k, q, kv, bl, causal, S, words=None, cut=(0, 0, 0)):
     n = k.splitkv_num_blocks(kv, bl)
     cost, sob, load = np.zeros(n, np.int64), np.zeros(n, np.int32), np.zeros(S, np.int64)
     work = np.zeros(words if words is not None else k.splitkv_work_words(n, len(q)), np.int32)
-    n_items, part_rows = k.splitkv_plan_batch(q, kv, bl, causal, S, cost, sob, load, work)
+    upi, slots, pieces = cut
+    n_items, part_rows = k.splitkv_plan_batch(q, kv, bl, causal, S, cost, sob, load, work, units_per_item=upi,
+                                              slots=slots, pieces=pieces)
     return cost, sob, load, work, n_items, part_rows
 
 
 def test_plan_batch_is_the_three_calls(k):
     """The one-call plan gives the oracle's costs and LPT plan and the same descriptor as
-    splitkv_build_work, on every workload and on fuzz cases."""
+    splitkv_build_work (splitkv_build_work_tail with a tail cut), on every workload and on fuzz
+    cases."""
     rng = random.Random(77)
     cases = [(*wl.lengths(w), w.block_len, w.causal, w.n_shards) for w in wl.WORKLOADS.values()]
     for _ in range(300):
@@ -399,6 +402,10 @@ def test_plan_batch_is_the_three_calls(k):
         ref_sob, ref_load = oracle.lpt_assign(ref_cost, S)
         assert cost.tolist() == ref_cost and sob.tolist() == ref_sob and load.tolist() == ref_load
         ref_work, ref_items, ref_rows = k.splitkv_build_work(q, kv, bl, cost, sob, S)
+        assert np.array_equal(work, ref_work) and (n_items, part_rows) == (ref_items, ref_rows)
+        cut = (rng.randint(1, 8), rng.randint(1, 40), rng.randint(2, 5))
+        *_, work, n_items, part_rows = _plan_batch(k, q, kv, bl, causal, S, cut=cut)
+        ref_work, ref_items, ref_rows = k.splitkv_build_work_tail(q, kv, bl, cost, sob, S, *cut)
         assert np.array_equal(work, ref_work) and (n_items, part_rows) == (ref_items, ref_rows)
 
 
