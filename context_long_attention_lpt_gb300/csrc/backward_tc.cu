@@ -450,7 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       has3 = has3 && ahead.next(&apos, &anv, &atok);
       ++t;
     }
-    // epilogue: dQ = scale * sum dS K
+    // epilogue: dQ = scale * sum dS K.  The destination rows are worked out
+    // while the last MMAs run (G divides 64, a power of two: shifts).
+    // (the row base goes through an opaque move, so the compiler cannot hoist this
+    // work into the tile loop, where it would hold registers across every tile)
+    int32_t row_base;
+    asm volatile("mov.b32 %0, %1;" : "=r"(row_base) : "r"(part_row));
+    const int lg = __ffs(G) - 1;
+    float4* dst_k[8];  // the staged path's row pieces: row 4 i + lane / 8 of this warp's 32
+    bool valid_k[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int32_t rk = rq * 32 + 4 * i + (lane >> 3);
+      valid_k[i] = rk < n_rows;
+      dst_k[i] = reinterpret_cast<float4*>(
+          dq_part + (static_cast<int64_t>(row_base + ((r0 + rk) >> lg)) * a.Hq + kvh * G + ((r0 + rk) & (G - 1))) * kD);
+    }
     if (ok && t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->o_done, 0))) ok = false;
     if (!ok && lane == 0) atomicOr(a.status, ptx::kStatusTimeout);
     tc::fence_after_sync();
@@ -460,14 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp passes 32 rows x 32 columns at a time through its 4 KB of it (16-byte
       // slot y of row k at y ^ (k & 7)) and stores whole 128-byte row pieces.
       float4* wst = reinterpret_cast<float4*>(sq + (hh * 4 + rq) * 4096);
-      int64_t orow_k[8];
-      bool valid_k[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int32_t rk = rq * 32 + 4 * i + (lane >> 3);
-        valid_k[i] = rk < n_rows;
-        orow_k[i] = static_cast<int64_t>(part_row + (r0 + rk) / G) * a.Hq + kvh * G + (r0 + rk) % G;
-      }
 #pragma unroll 1
       for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
         uint32_t acc[32];
@@ -482,8 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int kr = 4 * i + (lane >> 3), y = lane & 7;
-          if (valid_k[i])
-            reinterpret_cast<float4*>(dq_part + orow_k[i] * kD + 32 * q4)[y] = wst[kr * 8 + (y ^ (kr & 7))];
+          if (valid_k[i]) dst_k[i][8 * q4 + y] = wst[kr * 8 + (y ^ (kr & 7))];
         }
         __syncwarp();
       }
@@ -626,6 +632,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int32_t* sqrow = wv.seq(seq);
   const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
   const int32_t G = a.Hq / a.Hkv;
+  const int lg = __ffs(G) - 1;  // G divides 64: a power of two
   const int32_t rows = q_len * G;
   const int32_t n_rt = (rows + kRowsB - 1) / kRowsB;  // row tiles of the sequence
   // every key below kv_len gets a gradient (zero if no row sees it)
@@ -715,7 +722,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const int32_t row = r * kRowsB + 32 * u + lane;
           float L = -INFINITY, Dv = 0.f;
           if (row < rows) {
-            const int64_t g = static_cast<int64_t>(cu_q + row / G) * a.Hq + kvh * G + row % G;
+            const int64_t g = static_cast<int64_t>(cu_q + (row >> lg)) * a.Hq + kvh * G + (row & (G - 1));
             L = __ldg(lse + g);
             Dv = __ldg(delta + g);
           }
@@ -734,7 +741,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          const int32_t tok0 = cu_q + (r * kRowsB) / G;
+          const int32_t tok0 = cu_q + ((r * kRowsB) >> lg);
           ptx::mbar_arrive_expect_tx(&bar->qd_full[s], 2 * kTile64);
           ptx::tma_load_3d(sq + s * kTile64, &tmap_q, 0, kvh * G, tok0, &bar->qd_full[s]);
           ptx::tma_load_3d(sq + s * kTile64 + kHalf64, &tmap_q, 64, kvh * G, tok0, &bar->qd_full[s]);
