@@ -324,14 +324,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!a.fused) return;
 
   // ---- fused merge: the last CTA of this (sequence, K/V head) group merges ----
-  // Every thread publishes its partial rows before the group's ticket is taken
-  // (the usual fence-then-count pattern); no CTA ever waits for another.
+  // The CTA's partial rows are published before the group's ticket is taken:
+  // the barrier orders every thread's writes before thread 0's fence, whose
+  // release covers them (fence-then-count); no CTA ever waits for another.
   __shared__ int s_last;
-  __threadfence();
   __syncthreads();
   uint32_t* ticket = a.tickets + static_cast<int64_t>(seq) * a.Hkv + kvh;
   const int32_t p0 = __ldg(wv.seq(seq) + kSqItemPtr), p1 = __ldg(wv.seq(seq + 1) + kSqItemPtr);
   if (threadIdx.x == 0) {
+    __threadfence();
     const uint32_t taken = atomicAdd(ticket, 1u);
     s_last = taken == static_cast<uint32_t>(p1 - p0 - 1);
     __threadfence();
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int r = i / (kD / 4), c4 = i % (kD / 4);
     const int32_t tok = r / G, h = kvh * G + r % G;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
     for (int it = 0; it < n_it; ++it) {
       const float w = sm_w[it * R + r];
       const float4 x = __ldcg(reinterpret_cast<const float4*>(a.o_part + (static_cast<int64_t>(sm_pr[it] + tok) * a.Hq + h) * kD) + c4);
