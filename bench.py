@@ -553,11 +553,13 @@ def run_e2e(args, w, inp, run, dev, acc, bound):
         with torch.cuda.stream(copy_stream):
             if used[b]:
                 copy_stream.wait_event(ev_free[b])  # the step that last read this copy is done
+            # block costs, LPT, work lists and their upload, as every step: the upload goes on
+            # the copy stream ahead of the inputs, so it never queues behind the next step's copy
+            run.plan(stream=copy_stream)
             for k, v in host.items():
                 dbuf[b][k].copy_(v, non_blocking=True)
             ev_in[b].record(copy_stream)
         comp.wait_event(ev_in[b])
-        run.plan(stream=comp)  # block costs, LPT, work lists and their upload, as every step
         out, lse = run(dbuf[b]["q"], dbuf[b]["k_pool"], dbuf[b]["v_pool"], dbuf[b]["block_table"], w.scale,
                        out=dout[b][0], lse=dout[b][1], stream=comp)
         out_h.copy_(out, non_blocking=True)
