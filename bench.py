@@ -62,8 +62,8 @@ def parse_args(argv=None):
                          "reduction completion model (splitkv_plan_dcp)")
     ap.add_argument("--tail-pieces", type=int, default=None,
                     help="cut the items of the last partial wave of CTAs into this many pieces "
-                         "(splitkv_build_work_tail; 0: no cut; default: the runner's choice, 4 on the decode "
-                         "kernel and none elsewhere)")
+                         "(splitkv_build_work_tail; 0: no cut; default: the runner's choice, 4 when the last "
+                         "wave of CTAs is at most half full)")
     ap.add_argument("--item-blocks", type=int, default=0,
                     help="cut work items into runs of at most this many blocks (0: one item per shard and "
                          "sequence)")

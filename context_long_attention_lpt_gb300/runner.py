@@ -55,12 +55,9 @@ class SplitKVAttention:
         self._grad_pools = None
         self.total_q = sum(self.q_len)
         self.max_q_len = max(self.q_len) if self.q_len else 0
-        if self.tail_pieces is None:
-            # Default: cut the last partial wave into 4 pieces on the decode kernel, whose lone
-            # CTAs stream slowly (decode step: 184 -> 176 us); no cut elsewhere (the tensor-core
-            # kernel on 16 query rows: 200 -> 208 us with 4 pieces).
-            self.tail_pieces = 4 if self.item_blocks <= 0 and self.kernel_used() == _k.KERNEL_DECODE else 0
-        self.tail_pieces = int(self.tail_pieces)
+        # tail_pieces None: decided after the first plan (_choose_tail)
+        self._tail_auto = self.tail_pieces is None
+        self.tail_pieces = 0 if self._tail_auto else int(self.tail_pieces)
         self._q_len_np = np.asarray(self.q_len, dtype=np.int32)
         self._kv_len_np = np.asarray(self.kv_len, dtype=np.int32)
         # pinned staging buffers for the work list, used in turn, so planning the
@@ -82,6 +79,8 @@ class SplitKVAttention:
         self._last_use = [None, None]  # per buffer: event after the last device call that read it
         self._use_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self.plan()
+        if self._tail_auto and self._choose_tail():
+            self.plan()
 
     # host steps -------------------------------------------------------------
     def plan(self, stream=None):
@@ -153,6 +152,22 @@ class SplitKVAttention:
                 self._q_len_np, self._kv_len_np, self.block_len, self.block_cost, self.shard_of_block,
                 self.n_shards)
         return work
+
+    def _choose_tail(self):
+        """Default tail cut: when the launch's last wave of CTAs is at most half full, its
+        items are cut into 4 pieces (decode kernel: 184 -> 176 us; tensor-core kernel on the
+        1M-context shape: 2.64 -> 2.59 ms).  A fuller last wave gains nothing from the cut and
+        pays its extra partial rows (short query: 0.785 -> 0.798 ms; 16 query rows per K/V
+        head: 200 -> 208 us).  Returns whether a cut was chosen."""
+        if self.item_blocks > 0 or self.kernel_used() not in (_k.KERNEL_DECODE, _k.KERNEL_TC):
+            return False
+        per_item, slots = self._tail_slots()
+        units = self.n_items * per_item
+        rem = units % slots if slots > 0 else 0
+        if units > slots and 0 < rem <= slots // 2:
+            self.tail_pieces = 4
+            return True
+        return False
 
     def _tail_slots(self):
         """(CTAs per work item, resident CTAs) for the tail cut."""
