@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Split-KV attn fwd TFLOP/s & KV-read GB/s vs GB300 roofline, short-Q/long-KV"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SUSTAINED_REGION_S = 1.0  # timed regions at least this long compare with the sustained bf16 peak
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -374,8 +375,12 @@ def measure_forward(args, dctx, name, dev, headline=False):
         units_local, unit, scale = acc["kv_bytes"] * args.steps, "GB/s", 1e9
     else:
         achieved = acc["flops"] / (kernel_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
+        # A kernel timed inside a timed region of a second or more runs into the power limiter,
+        # as the sustained GEMM figure did; a shorter region is compared with the burst figure.
+        kind = "sustained" if local_s >= SUSTAINED_REGION_S else "burst"
+        peak = peaks["bf16_tflops_sustained"] if kind == "sustained" else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
         units_local, unit, scale = acc["flops"] * args.steps, "TFLOP/s", 1e12
     roof.update({"traffic": traffic_for(f"partial_{kname}", w.name), "kernel": f"partial_{kname}",
@@ -442,8 +447,11 @@ def measure_backward(args, dctx, name, dev):
     tc = K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, code) == K.KERNEL_TC
     achieved = flops / (local_s / n) / 1e12
     if tc:
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "peak_source": src,
+        kind = "sustained" if local_s >= SUSTAINED_REGION_S else "burst"
+        peak = peaks["bf16_tflops_sustained"] if kind == "sustained" else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"], "peak_source": src,
                 "note": "whole backward step: delta, dQ and dK/dV tensor-core kernels, dQ reduction"}
     else:
         roof = {"bound": "fp32_fma", "achieved": achieved, "unit": "TFLOP/s",
