@@ -63,13 +63,17 @@ __global__ void __launch_bounds__(kThreads)
 
   const int tid = threadIdx.x;
   const int32_t item = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
   const int32_t blk_off = __ldg(it + kItBlockOff), blk_cnt = __ldg(it + kItBlockCnt);
   const int32_t part_row = __ldg(it + kItPartRow);
-  const int32_t* sq = wv.seq(seq);
-  const int32_t cu_q = __ldg(sq + kSqCuQ), q_len = __ldg(sq + kSqQLen), kv_len = __ldg(sq + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {
+    if (tid == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
   if (rows == 0) return;
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(256)
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (gw >= static_cast<int64_t>(total_q) * Hq) return;
   const int32_t row = static_cast<int32_t>(gw / Hq), h = static_cast<int32_t>(gw % Hq);
-  const WorkView wv(work);
+  const WorkView wv(work, B);
   int32_t lo = 0, hi = B - 1;
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) >> 1;

@@ -176,12 +176,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t kvh = static_cast<int32_t>((u / units_per_item) % a.Hkv);
   const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(units_per_item) * a.Hkv));
 
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  // the header words and the item row are independent loads: one round trip
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
   const int32_t part_row = __ldg(it + kItPartRow);
-  const int32_t* sqrow = wv.seq(seq);
-  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
   const int32_t r0 = utile * kRows;
@@ -626,11 +631,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int32_t kvh = static_cast<int32_t>((blockIdx.x / key_split) % a.Hkv);
   const int32_t item = static_cast<int32_t>(blockIdx.x / (static_cast<int64_t>(key_split) * a.Hkv));
 
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
-  const int32_t* sqrow = wv.seq(seq);
-  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int lg = __ffs(G) - 1;  // G divides 64: a power of two
   const int32_t rows = q_len * G;

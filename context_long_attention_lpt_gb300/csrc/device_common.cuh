@@ -10,20 +10,39 @@
 
 namespace splitkv {
 
-// Read-only view of the work descriptor in device memory.
+// Read-only view of the work descriptor in device memory.  The sequence rows, item
+// rows and block lists sit at offsets fixed by B and n_items (work_layout.h), so
+// finding an item's row takes no load; only the per-sequence item lists, placed
+// after the block lists, are found through the header.
 struct WorkView {
   const int32_t* w;
-  __device__ __forceinline__ explicit WorkView(const int32_t* p) : w(p) {}
+  const int32_t* items_;
+  const int32_t* blocks_;
+  __device__ __forceinline__ WorkView(const int32_t* p, int32_t B, int32_t n_items)
+      : w(p), items_(p + work_off_items(B)), blocks_(p + work_off_blocks(B, n_items)) {}
+  // for the merges, which read sequence and item rows but no block list
+  __device__ __forceinline__ WorkView(const int32_t* p, int32_t B)
+      : w(p), items_(p + work_off_items(B)), blocks_(nullptr) {}
   __device__ __forceinline__ int32_t hdr(int i) const { return __ldg(w + i); }
   __device__ __forceinline__ const int32_t* item(int32_t i) const {
-    return w + hdr(kOffItems) + kItemWords * static_cast<int64_t>(i);
+    return items_ + kItemWords * static_cast<int64_t>(i);
   }
   __device__ __forceinline__ const int32_t* seq(int32_t b) const {
-    return w + hdr(kOffSeq) + kSeqWords * static_cast<int64_t>(b);
+    return w + work_off_seq() + kSeqWords * static_cast<int64_t>(b);
   }
-  __device__ __forceinline__ const int32_t* blocks() const { return w + hdr(kOffBlocks); }
+  __device__ __forceinline__ const int32_t* blocks() const { return blocks_; }
   __device__ __forceinline__ const int32_t* seq_items() const { return w + hdr(kOffSeqItems); }
 };
+
+// Status bit: the work descriptor was not built for the launch's B and n_items (its
+// magic word, B or n_items differ); the launch's CTAs did nothing.
+constexpr unsigned int kStatusBadWork = 8u;
+
+// Whether a descriptor header (magic word, B, n_items, loaded by the caller alongside
+// the item row, not before it) belongs to a launch over B sequences and n_items items.
+__device__ __forceinline__ bool work_matches(int32_t magic, int32_t b, int32_t n, int32_t B, int32_t n_items) {
+  return magic == kWorkMagic && b == B && n == n_items;
+}
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int32_t row = static_cast<int32_t>(gw / Hq);
   const int32_t h = static_cast<int32_t>(gw % Hq);
 
-  const WorkView wv(work);
+  const WorkView wv(work, B);
   // sequence of this row: last b with cu_q[b] <= row
   int32_t lo = 0, hi = B - 1;
   while (lo < hi) {

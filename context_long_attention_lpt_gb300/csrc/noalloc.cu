@@ -112,7 +112,9 @@ int check_descriptor(const int32_t* w, int64_t words, int32_t n_items, int32_t B
                 w[kNItems], n_items, w[kB], B, w[kTotalQ], total_q, w[kMaxQ], max_q_len);
   const int64_t off_seq = w[kOffSeq], off_items = w[kOffItems], off_blocks = w[kOffBlocks],
                 off_seq_items = w[kOffSeqItems], n_blocks = w[kNBlocks];
-  if (off_seq < kHeaderWords || off_items < 0 || off_blocks < 0 || off_seq_items < 0 || n_blocks < 0 ||
+  if (off_seq != work_off_seq() || off_items != work_off_items(B) || off_blocks != work_off_blocks(B, n_items))
+    return fail(SPLITKV_ERR_INVALID, "work descriptor sections are not where its B and n_items place them");
+  if (off_seq_items < 0 || n_blocks < 0 ||
       off_seq + (static_cast<int64_t>(B) + 1) * kSeqWords > words ||
       off_items + static_cast<int64_t>(n_items) * kItemWords > words || off_blocks + n_blocks > words ||
       off_seq_items + n_items > words)
@@ -123,8 +125,9 @@ int check_descriptor(const int32_t* w, int64_t words, int32_t n_items, int32_t B
     const int32_t seq = it[kItSeq], prow = it[kItPartRow];
     if (seq < 0 || seq >= B || prow < 0)
       return fail(SPLITKV_ERR_INVALID, "work item %d has sequence %d / partial row %d out of range", i, seq, prow);
-    const int32_t lq = w[off_seq + static_cast<int64_t>(seq) * kSeqWords + kSqQLen];
-    if (lq < 0 || lq > max_q_len) return fail(SPLITKV_ERR_INVALID, "sequence %d has q_len %d", seq, lq);
+    const int32_t lq = it[kItQLen];  // the kernels take the item row's copy of q_len
+    if (lq < 0 || lq > max_q_len || lq != w[off_seq + static_cast<int64_t>(seq) * kSeqWords + kSqQLen])
+      return fail(SPLITKV_ERR_INVALID, "work item %d has q_len %d (sequence %d)", i, lq, seq);
     need = std::max<int64_t>(need, static_cast<int64_t>(prow) + lq);
   }
   *rows_needed = need;

@@ -95,13 +95,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int32_t item = blockIdx.x / a.Hkv;
   const int32_t kvh = blockIdx.x % a.Hkv;
 
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  // the header words and the item row are independent loads: one round trip
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
   const int32_t blk_off = __ldg(it + kItBlockOff), blk_cnt = __ldg(it + kItBlockCnt);
   const int32_t part_row = __ldg(it + kItPartRow);
-  const int32_t* sq = wv.seq(seq);
-  const int32_t cu_q = __ldg(sq + kSqCuQ), q_len = __ldg(sq + kSqQLen), kv_len = __ldg(sq + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
   if (rows == 0) return;
@@ -330,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_last;
   __syncthreads();
   uint32_t* ticket = a.tickets + static_cast<int64_t>(seq) * a.Hkv + kvh;
-  const int32_t p0 = __ldg(wv.seq(seq) + kSqItemPtr), p1 = __ldg(wv.seq(seq + 1) + kSqItemPtr);
+  const WorkView mv(a.work, a.B, a.n_items);  // rebuilt from the arguments: nothing kept live across the loop
+  const int32_t p0 = __ldg(mv.seq(seq) + kSqItemPtr), p1 = __ldg(mv.seq(seq + 1) + kSqItemPtr);
   if (threadIdx.x == 0) {
     __threadfence();
     const uint32_t taken = atomicAdd(ticket, 1u);
@@ -341,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!s_last) return;
   // Merge: all LSEs of the group at once, weights per row, then the weighted sum
   // of the partial rows with independent loads (they sit in L2, just written).
-  const int32_t* seq_items = wv.seq_items();
+  const int32_t* seq_items = mv.seq_items();
   const int32_t n_it = p1 - p0;
   float* sm_w = reinterpret_cast<float*>(smem);            // [n_it][R] weights
   int32_t* sm_pr = reinterpret_cast<int32_t*>(sm_w + kMaxFusedItems * R);  // [n_it] partial rows
-  for (int i = threadIdx.x; i < n_it; i += kThreads) sm_pr[i] = __ldg(wv.item(__ldg(seq_items + p0 + i)) + kItPartRow);
+  for (int i = threadIdx.x; i < n_it; i += kThreads) sm_pr[i] = __ldg(mv.item(__ldg(seq_items + p0 + i)) + kItPartRow);
   __syncthreads();
   for (int i = threadIdx.x; i < n_it * rows; i += kThreads) {
     const int it = i / rows, r = i % rows;

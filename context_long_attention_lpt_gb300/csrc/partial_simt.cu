@@ -41,13 +41,17 @@ __global__ void __launch_bounds__(kThreads)
   const int32_t kvh = static_cast<int32_t>((u / tiles_per_item) % a.Hkv);
   const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(tiles_per_item) * a.Hkv));
 
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
   const int32_t blk_off = __ldg(it + kItBlockOff), blk_cnt = __ldg(it + kItBlockCnt);
   const int32_t part_row = __ldg(it + kItPartRow);
-  const int32_t* sq = wv.seq(seq);
-  const int32_t cu_q = __ldg(sq + kSqCuQ), q_len = __ldg(sq + kSqQLen), kv_len = __ldg(sq + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
   const int32_t r0 = tile * kRows;

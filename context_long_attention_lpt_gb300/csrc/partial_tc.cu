@@ -171,13 +171,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t kvh = static_cast<int32_t>((u / units_per_item) % a.Hkv);
   const int32_t item = static_cast<int32_t>(u / (static_cast<int64_t>(units_per_item) * a.Hkv));
 
-  const WorkView wv(a.work);
+  const WorkView wv(a.work, a.B, a.n_items);
   const int32_t* it = wv.item(item);
+  // the header words and the item row are independent loads: one round trip
+  const int32_t h_magic = wv.hdr(kMagic), h_b = wv.hdr(kB), h_n = wv.hdr(kNItems);
   const int32_t seq = __ldg(it + kItSeq);
   const int32_t blk_off = __ldg(it + kItBlockOff), blk_cnt = __ldg(it + kItBlockCnt);
   const int32_t part_row = __ldg(it + kItPartRow);
-  const int32_t* sqrow = wv.seq(seq);
-  const int32_t cu_q = __ldg(sqrow + kSqCuQ), q_len = __ldg(sqrow + kSqQLen), kv_len = __ldg(sqrow + kSqKvLen);
+  const int32_t cu_q = __ldg(it + kItCuQ), q_len = __ldg(it + kItQLen), kv_len = __ldg(it + kItKvLen);
+  if (!work_matches(h_magic, h_b, h_n, a.B, a.n_items)) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadWork);
+    return;
+  }
   const int32_t G = a.Hq / a.Hkv;
   const int32_t rows = q_len * G;
   const int32_t r0 = utile * kM;
@@ -637,11 +642,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t um = blockIdx.x;
       const int32_t m_utile = static_cast<int32_t>(um % units_per_item);
       const int32_t m_kvh = static_cast<int32_t>((um / units_per_item) % a.Hkv);
-      const int32_t m_seq = __ldg(wv.item(static_cast<int32_t>(um / (static_cast<int64_t>(units_per_item) * a.Hkv))) + kItSeq);
-      const int32_t m_cu = __ldg(wv.seq(m_seq) + kSqCuQ);
+      const WorkView mv(a.work, a.B, a.n_items);  // rebuilt from the arguments: nothing kept live across the loop
+      const int32_t* m_it = mv.item(static_cast<int32_t>(um / (static_cast<int64_t>(units_per_item) * a.Hkv)));
+      const int32_t m_seq = __ldg(m_it + kItSeq);
+      const int32_t m_cu = __ldg(m_it + kItCuQ);
       const int32_t m_r0 = m_utile * kM;
-      const int32_t m_rows = min(kM, __ldg(wv.seq(m_seq) + kSqQLen) * G - m_r0);
-      const int32_t p0 = __ldg(wv.seq(m_seq) + kSqItemPtr), p1 = __ldg(wv.seq(m_seq + 1) + kSqItemPtr);
+      const int32_t m_rows = min(kM, __ldg(m_it + kItQLen) * G - m_r0);
+      const int32_t p0 = __ldg(mv.seq(m_seq) + kSqItemPtr), p1 = __ldg(mv.seq(m_seq + 1) + kSqItemPtr);
       uint32_t* ticket = a.tickets + (static_cast<int64_t>(m_seq) * a.Hkv + m_kvh) * units_per_item + m_utile;
       if (threadIdx.x == 0) {
         const uint32_t taken = atomicAdd(ticket, 1u);
@@ -655,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one warp per (token, head) row of the unit, the partials read through L2
         for (int32_t r = warp; r < m_rows; r += merge_threads / 32) {
           const int32_t rr = m_r0 + r, tok = rr / G, h = m_kvh * G + rr % G;
-          merge_row<__nv_bfloat16, kD, true>(a.o_part, a.lse_part, wv, p0, p1, tok, h, a.Hq,
+          merge_row<__nv_bfloat16, kD, true>(a.o_part, a.lse_part, mv, p0, p1, tok, h, a.Hq,
                                              static_cast<int64_t>(m_cu + tok) * a.Hq + h,
                                              static_cast<__nv_bfloat16*>(a.out), a.lse_out);
         }

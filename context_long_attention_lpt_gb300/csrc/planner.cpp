@@ -338,9 +338,9 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
   }
 
   const int32_t n_items = static_cast<int32_t>(items.size());
-  const int64_t off_seq = kHeaderWords;
-  const int64_t off_items = off_seq + kSeqWords * (static_cast<int64_t>(B) + 1);
-  const int64_t off_blocks = off_items + kItemWords * static_cast<int64_t>(n_items);
+  const int64_t off_seq = work_off_seq();
+  const int64_t off_items = work_off_items(B);
+  const int64_t off_blocks = work_off_blocks(B, n_items);
   const int64_t off_seq_items = off_blocks + n_blocks;
   std::memset(work, 0, sizeof(int32_t) * static_cast<size_t>(off_seq_items + n_items));
 
@@ -361,6 +361,8 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
 
   int64_t part_row = 0;
   int64_t blk_cursor = 0;
+  std::vector<int32_t> cu_q(static_cast<size_t>(B), 0);
+  for (int32_t b = 1; b < B; ++b) cu_q[b] = cu_q[b - 1] + q_len[b - 1];
   std::vector<int32_t> rank_of(items.size());
   for (int32_t r = 0; r < n_items; ++r) {
     const Item& it = items[order[r]];
@@ -372,6 +374,9 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
     w[kItBlockCnt] = static_cast<int32_t>(it.count);
     if (part_row > INT32_MAX) return fail(SPLITKV_ERR_UNSUPPORTED, "partial rows exceed int32");
     w[kItPartRow] = static_cast<int32_t>(part_row);
+    w[kItQLen] = q_len[it.seq];
+    w[kItKvLen] = kv_len[it.seq];
+    w[kItCuQ] = cu_q[it.seq];
     w[kItCostLo] = static_cast<int32_t>(static_cast<uint64_t>(it.cost) & 0xffffffffu);
     w[kItCostHi] = static_cast<int32_t>(static_cast<uint64_t>(it.cost) >> 32);
     for (int64_t k = 0; k < it.count; ++k) work[off_blocks + blk_cursor + k] = blk_of[idx[it.first + k]];

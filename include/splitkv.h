@@ -115,16 +115,24 @@ int64_t splitkv_work_words(int64_t n_blocks, int32_t B);
  * sequence) pair that holds at least one block, and writes the int32 work
  * descriptor consumed by splitkv_attn_partial / splitkv_merge (host buffer of
  * work_words words; the caller copies it to the device).  Layout:
- *   [0..15]  header: magic 0x534B5631, B, n_items, n_shards, block_len,
+ *   [0..15]  header: magic 0x534B5632, B, n_items, n_shards, block_len,
  *            total_q, max_q_len, off_seq, off_items, off_blocks, off_seq_items,
  *            n_blocks, 0...
- *   off_seq        (B+1) x 4: {cu_q[b], q_len[b], kv_len[b], seq_item_ptr[b]};
+ *   off_seq = 16   (B+1) x 4: {cu_q[b], q_len[b], kv_len[b], seq_item_ptr[b]};
  *                  row B = {total_q, 0, 0, n_items}
- *   off_items      n_items x 8: {shard, seq, block_off, block_cnt, part_row,
- *                  cost_lo, cost_hi, 0}; items sorted by cost (largest first,
- *                  then shard, then sequence) - the launch order
- *   off_blocks     n_blocks: logical block indices, grouped by item, ascending
- *   off_seq_items  n_items: item indices grouped by sequence, ascending shard
+ *   off_items = 16 + 4(B+1)
+ *                  n_items x 12: {shard, seq, block_off, block_cnt, part_row,
+ *                  q_len[seq], kv_len[seq], cu_q[seq], cost_lo, cost_hi, 0, 0};
+ *                  items sorted by cost (largest first, then shard, then
+ *                  sequence) - the launch order
+ *   off_blocks = off_items + 12 n_items
+ *                  n_blocks: logical block indices, grouped by item, ascending
+ *   off_seq_items = off_blocks + n_blocks
+ *                  n_items: item indices grouped by sequence, ascending shard
+ * The kernels find the sequence rows, item rows and block lists at these fixed
+ * offsets from their B and n_items arguments (a CTA's first read is its item
+ * row, which repeats its sequence's lengths); a launch whose B or n_items
+ * differ from the header's does no work and sets bit 3 of the status word.
  * Item i's partial output occupies rows part_row .. part_row+q_len[seq]-1 of
  * the partial buffers; *part_rows (out) is the total row count (sum over items
  * of q_len of its sequence) and *n_items (out) the number of items. */
@@ -362,8 +370,10 @@ int splitkv_dq_reduce(const float* dq_part, int64_t part_rows, const int32_t* wo
 
 /* Reads and optionally clears the device status word: bit 0, a logical block
  * past max_blocks_per_seq or a block-table entry outside the pool was skipped;
- * bit 1, a work item's partial rows fell outside part_rows (item skipped).
- * Synchronises the device. */
+ * bit 1, a work item's partial rows fell outside part_rows (item skipped);
+ * bit 2, a wait of a pipelined kernel ran out its time limit (that launch's
+ * outputs are not valid); bit 3, a work descriptor did not match the launch's
+ * B and n_items (the launch did nothing).  Synchronises the device. */
 int splitkv_device_status(uint32_t* status, int32_t clear);
 
 /* Message of the last failed call on this thread ("" if none). */

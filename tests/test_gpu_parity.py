@@ -70,7 +70,7 @@ def test_partials_match_oracle_partials(name, kernel):
             inp.kv_len, w.block_len, w.causal, w.scale)
     cache = {}
     for i in range(n_items):
-        shard, seq, _, _, prow = work[off_items + 8 * i: off_items + 8 * i + 5].tolist()
+        shard, seq, _, _, prow = work[off_items + 12 * i: off_items + 12 * i + 5].tolist()
         if shard not in cache:
             cache[shard] = oracle.partial(*args, key_blocks=sets[shard])
         o_ref, l_ref = cache[shard]
@@ -140,6 +140,46 @@ def test_out_of_range_block_is_reported_not_read():
     torch.cuda.synchronize()
     eo, el = max_errors(out, lse, *full_reference(inp))
     assert_close(w, eo, el)
+
+
+@pytest.mark.parametrize("name,kernel", [("decode_small", K.KERNEL_AUTO), ("decode_small", K.KERNEL_SIMT),
+                                         ("varlen_small", K.KERNEL_AUTO), ("shortq_small", K.KERNEL_AUTO),
+                                         ("tiny", K.KERNEL_AUTO)])
+def test_descriptor_of_another_launch_is_reported_not_used(name, kernel):
+    """A launch told fewer items or sequences than its descriptor was built for finds the rows
+    where its own arguments place them, sees the header disagree, writes nothing and sets bit 3
+    of the status word (forward and backward kernels)."""
+    w = SMALL[name]
+    inp = wl.make_inputs(w, device="cuda")
+    run = SplitKVAttention(inp.q_len, inp.kv_len, w.block_len, w.causal, w.n_shards, w.Hq, w.Hkv, w.d,
+                           inp.q.dtype, kernel=kernel, tail_pieces=0)
+    out, lse = run(inp.q, inp.k_pool, inp.v_pool, inp.block_table, w.scale)
+    torch.cuda.synchronize()
+    assert K.splitkv_device_status(clear=True) == 0 and run.n_items >= 2
+    dout = torch.ones_like(out)
+    delta = torch.zeros((run.total_q, w.Hq), dtype=torch.float32, device="cuda")
+    cases = [(run.n_items - 1, run.B)] + ([(run.n_items, run.B - 1)] if run.B > 1 else [])
+    for n_items, B in cases:
+        run._o_part.fill_(7.0)
+        K.splitkv_attn_partial(inp.q, inp.k_pool, inp.v_pool, inp.block_table, run.work_device, n_items, B,
+                               run.total_q, run.max_q_len, w.block_len, w.scale, w.causal, run._o_part,
+                               run._lse_part, kernel=kernel)
+        torch.cuda.synchronize()
+        assert K.splitkv_device_status(clear=True) == 8, (n_items, B)
+        assert bool((run._o_part == 7.0).all())
+        dq_part = torch.full((max(run.part_rows, 1), w.Hq, w.d), 7.0, dtype=torch.float32, device="cuda")
+        dk = torch.full(tuple(inp.k_pool.shape), 7.0, dtype=torch.float32, device="cuda")
+        dv = torch.full(tuple(inp.v_pool.shape), 7.0, dtype=torch.float32, device="cuda")
+        K.splitkv_attn_backward(inp.q, inp.k_pool, inp.v_pool, inp.block_table, run.work_device, n_items, B,
+                                run.total_q, run.max_q_len, w.block_len, w.scale, w.causal, dout, lse, delta,
+                                dq_part, dk, dv)
+        torch.cuda.synchronize()
+        assert K.splitkv_device_status(clear=True) == 8, (n_items, B)
+        assert bool((dk == 7.0).all()) and bool((dv == 7.0).all())
+        # the CUDA-core backward clears the partial dQ rows before its atomic adds
+        code = K.SPLITKV_F32 if w.dtype == "f32" else K.SPLITKV_BF16
+        tc = K.splitkv_backward_kernel(w.Hq, w.Hkv, w.d, w.block_len, code) == K.KERNEL_TC
+        assert bool((dq_part == (7.0 if tc else 0.0)).all())
 
 
 def test_bad_arguments_raise_before_launch():

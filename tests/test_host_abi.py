@@ -86,11 +86,14 @@ def test_fuzz_plans_with_many_ties(k):
 
 def _decode_work(work):
     hdr = work[:16]
-    assert hdr[0] == 0x534B5631
+    assert hdr[0] == 0x534B5632
     B, n_items, n_shards, bl, total_q, max_q = hdr[1:7]
     off_seq, off_items, off_blocks, off_seq_items, n_blocks = hdr[7:12]
+    # the sections sit where B and n_items place them (the kernels rely on it)
+    assert off_seq == 16 and off_items == 16 + 4 * (B + 1) and off_blocks == off_items + 12 * n_items
+    assert off_seq_items == off_blocks + n_blocks
     seqs = work[off_seq: off_seq + 4 * (B + 1)].reshape(B + 1, 4)
-    items = work[off_items: off_items + 8 * n_items].reshape(n_items, 8)
+    items = work[off_items: off_items + 12 * n_items].reshape(n_items, 12)
     blocks = work[off_blocks: off_blocks + n_blocks]
     seq_items = work[off_seq_items: off_seq_items + n_items]
     return dict(B=B, n_items=n_items, total_q=total_q, max_q=max_q, seqs=seqs, items=items,
@@ -112,7 +115,8 @@ def test_work_lists_cover_the_plan(k, name):
     item_costs = []
     gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
     for i, it in enumerate(d["items"]):
-        shard, seq, off, cnt, prow, clo, chi, _ = it.tolist()
+        shard, seq, off, cnt, prow, iq, ikv, icu, clo, chi, z0, z1 = it.tolist()
+        assert (iq, ikv, icu, z0, z1) == (q[seq], kv[seq], sum(q[:seq]), 0, 0)  # the sequence's row, copied
         blks = d["blocks"][off: off + cnt].tolist()
         assert blks == sets[shard][seq] and cnt > 0
         for j in blks:
@@ -154,7 +158,8 @@ def test_split_work_lists_cover_the_plan(k, name, max_blocks):
     gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
     item_costs = []
     for it in d["items"]:
-        shard, seq, off, cnt, prow, clo, chi, _ = it.tolist()
+        shard, seq, off, cnt, prow, iq, ikv, icu, clo, chi = it.tolist()[:10]
+        assert (iq, ikv, icu) == (q[seq], kv[seq], sum(q[:seq]))
         assert 0 < cnt <= max_blocks
         blks = d["blocks"][off: off + cnt].tolist()
         got.setdefault((shard, seq), []).append(blks)
@@ -347,7 +352,8 @@ def test_tail_work_lists(k, name, upi, slots, pieces):
     gbase = np.cumsum([0] + [-(-n // w.block_len) for n in kv])
     got = {}
     for it, (shard, seq, blks) in zip(d["items"], want):
-        s_, b_, off, cnt, prow, clo, chi, _ = it.tolist()
+        s_, b_, off, cnt, prow, iq, ikv, icu, clo, chi = it.tolist()[:10]
+        assert (iq, ikv, icu) == (q[seq], kv[seq], sum(q[:seq]))
         assert (s_, b_) == (shard, seq) and d["blocks"][off: off + cnt].tolist() == blks
         assert prow == rows
         rows += q[seq]
