@@ -28,6 +28,19 @@ def k():
     return splitkv
 
 
+def test_a_missing_library_raises_and_nothing_falls_back(k, monkeypatch, tmp_path):
+    """Without the built library every entry point, host planning included, raises: the
+    package has no CPU fallback for any step of the path."""
+    from context_long_attention_lpt_gb300 import runner
+
+    monkeypatch.setattr(k, "_LIB_PATH", str(tmp_path / "libsplitkv.so"))
+    monkeypatch.setattr(k, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        k.splitkv_block_costs([4], [8], 4, True)
+    with pytest.raises(RuntimeError, match="not found"):
+        runner.SplitKVAttention([4], [8], 4, True, 2, 4, 4, 64, None, device="cpu")
+
+
 def _header_symbols():
     text = open(os.path.join(ROOT, "include", "splitkv.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
