@@ -99,25 +99,49 @@ extern "C" int splitkv_block_costs(const int32_t* q_len, const int32_t* kv_len, 
 
 namespace {
 
-// Longest first; equal costs keep ascending block index.  When every cost and
-// index fits in 32 bits the pair is packed into one 64-bit key (complemented
-// cost high, index low) so the sort compares plain integers.
-void lpt_order(const int64_t* block_cost, int64_t n_blocks, std::vector<int64_t>& order) {
-  order.resize(static_cast<size_t>(n_blocks));
-  int64_t max_cost = 0;
-  for (int64_t g = 0; g < n_blocks; ++g) max_cost = std::max(max_cost, block_cost[g]);
-  if (max_cost <= 0xffffffffLL && n_blocks <= 0xffffffffLL) {
-    std::vector<uint64_t> key(static_cast<size_t>(n_blocks));
-    for (int64_t g = 0; g < n_blocks; ++g)
-      key[g] = ((0xffffffffull - static_cast<uint64_t>(block_cost[g])) << 32) | static_cast<uint64_t>(g);
-    if (!std::is_sorted(key.begin(), key.end())) std::sort(key.begin(), key.end());  // equal costs: sorted
-    for (int64_t i = 0; i < n_blocks; ++i) order[i] = static_cast<int64_t>(key[i] & 0xffffffffull);
-    return;
+// Indices 0..n-1 by (signed 64-bit) key descending, equal keys in ascending index
+// order: a least-significant-digit radix sort (8-bit digits) of the complemented keys.  Each pass is
+// stable, so indices of equal keys keep the ascending order they start in; digits
+// that are the same in every key are skipped (costs usually span a few bytes).
+// O(n) per pass, against O(n log n) comparisons of a comparison sort.
+template <typename Index, typename KeyOf>
+void order_desc_stable(int64_t n, KeyOf key_of, std::vector<Index>& order) {
+  // per-thread buffers kept across calls: a planner run each step reuses their pages
+  thread_local std::vector<uint64_t> key, key2;
+  thread_local std::vector<Index> order2;
+  order.resize(static_cast<size_t>(n));
+  key.resize(static_cast<size_t>(n));
+  uint64_t any = 0, all = ~uint64_t{0};
+  bool sorted = true;
+  for (int64_t i = 0; i < n; ++i) {
+    // sign bit flipped: unsigned order = signed order; complemented: descending
+    key[i] = ~(static_cast<uint64_t>(static_cast<int64_t>(key_of(i))) ^ (uint64_t{1} << 63));
+    any |= key[i];
+    all &= key[i];
+    order[i] = static_cast<Index>(i);
+    if (i > 0 && key[i] < key[i - 1]) sorted = false;
   }
-  for (int64_t g = 0; g < n_blocks; ++g) order[g] = g;
-  std::sort(order.begin(), order.end(), [&](int64_t x, int64_t y) {
-    return block_cost[x] != block_cost[y] ? block_cost[x] > block_cost[y] : x < y;
-  });
+  if (sorted) return;  // already non-increasing: the index order is the answer
+  order2.resize(static_cast<size_t>(n));
+  key2.resize(static_cast<size_t>(n));
+  for (int shift = 0; shift < 64; shift += 8) {
+    if ((((any ^ all) >> shift) & 0xffu) == 0) continue;  // this digit is equal in every key
+    int64_t start[257] = {0};
+    for (int64_t i = 0; i < n; ++i) ++start[((key[i] >> shift) & 0xffu) + 1];
+    for (int d = 0; d < 256; ++d) start[d + 1] += start[d];
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t at = start[(key[i] >> shift) & 0xffu]++;
+      order2[at] = order[i];
+      key2[at] = key[i];
+    }
+    order.swap(order2);
+    key.swap(key2);
+  }
+}
+
+// Longest first; equal costs keep ascending block index.
+void lpt_order(const int64_t* block_cost, int64_t n_blocks, std::vector<int64_t>& order) {
+  order_desc_stable<int64_t>(n_blocks, [&](int64_t g) { return block_cost[g]; }, order);
 }
 
 // Each block in `order` goes to the least-loaded shard, the smallest
@@ -182,7 +206,7 @@ extern "C" int splitkv_plan(const int64_t* block_cost, int64_t n_blocks, int32_t
   for (int64_t g = 0; g < n_blocks; ++g)
     if (block_cost[g] < 0) return fail(SPLITKV_ERR_INVALID, "negative cost at block %lld", (long long)g);
 
-  std::vector<int64_t> order;
+  thread_local std::vector<int64_t> order;  // kept across calls (see order_desc_stable)
   lpt_order(block_cost, n_blocks, order);
   lpt_assign_sorted(order, block_cost, n_shards, shard_of_block, shard_load);
   splitkv::clear_error();
@@ -247,7 +271,10 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
                 (long long)work_words, (long long)need);
 
   // Global block g -> (sequence, logical block).
-  std::vector<int32_t> seq_of(static_cast<size_t>(n_blocks)), blk_of(static_cast<size_t>(n_blocks));
+  // per-thread buffers kept across calls (a planner run each step reuses their pages)
+  thread_local std::vector<int32_t> seq_of, blk_of;
+  seq_of.resize(static_cast<size_t>(n_blocks));
+  blk_of.resize(static_cast<size_t>(n_blocks));
   int64_t g = 0;
   int64_t total_q = 0;
   int32_t max_q = 0;
@@ -271,10 +298,12 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
   // Group blocks by (shard, sequence); within a group blocks stay ascending.  A
   // counting sort on shard * B + sequence when there are not many more groups
   // than blocks, else a stable comparison sort: the same order either way.
-  std::vector<int64_t> idx(static_cast<size_t>(n_blocks));
+  thread_local std::vector<int64_t> idx;
+  idx.resize(static_cast<size_t>(n_blocks));
   const int64_t groups = static_cast<int64_t>(n_shards) * B;
   if (groups <= 4 * n_blocks + 4096) {
-    std::vector<int64_t> start(static_cast<size_t>(groups) + 1, 0);
+    thread_local std::vector<int64_t> start;
+    start.assign(static_cast<size_t>(groups) + 1, 0);
     for (int64_t i = 0; i < n_blocks; ++i) ++start[static_cast<int64_t>(shard_of_block[i]) * B + seq_of[i] + 1];
     for (int64_t k = 0; k < groups; ++k) start[k + 1] += start[k];
     for (int64_t i = 0; i < n_blocks; ++i) idx[start[static_cast<int64_t>(shard_of_block[i]) * B + seq_of[i]]++] = i;
@@ -289,7 +318,8 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
     int32_t shard, seq;
     int64_t first, count, cost;
   };
-  std::vector<Item> items;
+  thread_local std::vector<Item> items;
+  items.clear();
   for (int64_t i = 0; i < n_blocks;) {
     int64_t j = i;
     Item it{shard_of_block[idx[i]], seq_of[idx[i]], i, 0, 0};
@@ -303,11 +333,8 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
     i = j;
   }
   // Launch order: largest item first, then shard, then sequence.
-  std::vector<int32_t> order(items.size());
-  for (size_t i = 0; i < items.size(); ++i) order[i] = static_cast<int32_t>(i);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
-    return items[x].cost > items[y].cost;
-  });
+  thread_local std::vector<int32_t> order;
+  order_desc_stable<int32_t>(static_cast<int64_t>(items.size()), [&](int64_t i) { return items[i].cost; }, order);
   // Tail cut: the items of the last partial wave, in launch order, each become up
   // to `pieces` items of consecutive blocks, launched last (piece order kept).
   const int64_t units = static_cast<int64_t>(items.size()) * cut.units_per_item;
@@ -363,7 +390,8 @@ int build_work(const int32_t* q_len, const int32_t* kv_len, int32_t B, int32_t b
   int64_t blk_cursor = 0;
   std::vector<int32_t> cu_q(static_cast<size_t>(B), 0);
   for (int32_t b = 1; b < B; ++b) cu_q[b] = cu_q[b - 1] + q_len[b - 1];
-  std::vector<int32_t> rank_of(items.size());
+  thread_local std::vector<int32_t> rank_of;
+  rank_of.resize(items.size());
   for (int32_t r = 0; r < n_items; ++r) {
     const Item& it = items[order[r]];
     rank_of[order[r]] = r;
