@@ -97,6 +97,20 @@ def test_fuzz_plans_with_many_ties(k):
         assert sob.tolist() == rsob and load.tolist() == rload, case
 
 
+def test_fuzz_plans_with_costs_across_many_bytes(k):
+    """Costs whose differences sit in different bytes (up to 2^50, so every radix digit of
+    the LPT order is exercised), with repeated values and zeros: the plan is the oracle's."""
+    rng = random.Random(7)
+    for case in range(600):
+        n = rng.randint(0, 300)
+        pool = [rng.randint(0, 1 << rng.choice([4, 12, 20, 33, 50])) for _ in range(rng.randint(1, 12))]
+        costs = [rng.choice(pool + [0]) for _ in range(n)]
+        S = rng.randint(1, 20)
+        sob, load = k.splitkv_plan(np.array(costs, dtype=np.int64), S)
+        rsob, rload = oracle.lpt_assign(costs, S)
+        assert sob.tolist() == rsob and load.tolist() == rload, case
+
+
 def _decode_work(work):
     hdr = work[:16]
     assert hdr[0] == 0x534B5632
@@ -143,6 +157,9 @@ def test_work_lists_cover_the_plan(k, name):
     assert len(seen) == len(costs)
     assert rows == part_rows
     assert item_costs == sorted(item_costs, reverse=True)
+    # launch order: cost descending, then shard, then sequence
+    keys = [(-c, int(it[0]), int(it[1])) for c, it in zip(item_costs, d["items"])]
+    assert keys == sorted(keys)
     # per-sequence item lists: every item of the sequence, ascending shard
     for b in range(len(q)):
         p0, p1 = d["seqs"][b, 3], d["seqs"][b + 1, 3]
