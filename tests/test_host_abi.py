@@ -111,6 +111,35 @@ def test_fuzz_plans_with_costs_across_many_bytes(k):
         assert sob.tolist() == rsob and load.tolist() == rload, case
 
 
+def test_fuzz_work_lists_launch_order(k):
+    """Random batches: the items are the plan's (shard, sequence) pairs, launched by cost
+    descending, then shard, then sequence."""
+    rng = random.Random(31)
+    for case in range(300):
+        B = rng.randint(1, 6)
+        causal = rng.random() < 0.6
+        q = [rng.randint(0, 300) for _ in range(B)]
+        kv = [qq + rng.randint(0 if qq else 1, 5000) for qq in q]
+        bl = rng.choice([16, 64, 128, 1024])
+        S = rng.randint(1, 16)
+        costs = k.splitkv_block_costs(q, kv, bl, causal)
+        sob, _ = k.splitkv_plan(costs, S)
+        work, n_items, _ = k.splitkv_build_work(q, kv, bl, costs, sob, S)
+        d = _decode_work(work)
+        gbase = np.cumsum([0] + [-(-n // bl) for n in kv])
+        pairs = {}
+        for g in range(len(costs)):
+            b = int(np.searchsorted(gbase, g, side="right") - 1)
+            pairs.setdefault((int(sob[g]), b), 0)
+            pairs[(int(sob[g]), b)] += int(costs[g])
+        want = sorted(((-c, s_, b) for (s_, b), c in pairs.items()))
+        got = []
+        for it in d["items"]:
+            shard, seq, clo, chi = int(it[0]), int(it[1]), int(it[8]), int(it[9])
+            got.append((-((clo & 0xFFFFFFFF) | (chi << 32)), shard, seq))
+        assert got == want, case
+
+
 def _decode_work(work):
     hdr = work[:16]
     assert hdr[0] == 0x534B5632
